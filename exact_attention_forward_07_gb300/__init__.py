@@ -1,0 +1,155 @@
+"""Exact attention forward for NVIDIA GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI in include/fa.h (libfa_gb300.so, built
+in-tree by ``build.py``).  Every step of the computation runs in the CUDA
+kernels of that library; this module only checks tensor properties and
+passes pointers, sizes and the current CUDA stream.  There is no CPU or
+PyTorch fallback: if the library is missing the import of the binding
+fails loudly.
+
+    from exact_attention_forward_07_gb300 import forward
+    o, lse = forward(q, k, v, causal=True)          # q, k, v: [B,H,N,d] cuda
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+__all__ = ["FaError", "fa_fwd", "fa_fwd_fp16", "fa_get_status", "fa_strerror", "fa_version",
+           "forward", "library_path", "lib"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
+
+FA_OK = 0
+FA_ERR_NULL = -1
+FA_ERR_SHAPE = -2
+FA_ERR_HEADDIM = -3
+FA_ERR_UNSUPPORTED_N = -4
+FA_ERR_ALIGN = -5
+FA_ERR_SCALE = -6
+FA_ERR_DEVICE = -7
+FA_ERR_CUDA = -8
+FA_ERR_TIMEOUT = -9
+FA_ERR_ALIAS = -10
+FA_MAX_N = 1 << 20
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, where: str = ""):
+        self.code = code
+        msg = fa_strerror(code)
+        if code == FA_ERR_CUDA:
+            msg += f" (cudaError {lib().fa_last_cuda_error()})"
+        super().__init__(f"{where}: {msg} [{code}]" if where else f"{msg} [{code}]")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded libfa_gb300.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(
+                f"{_LIB_PATH} is missing: build it with "
+                "`python -m exact_attention_forward_07_gb300.build` (needs nvcc)")
+        L = ctypes.CDLL(_LIB_PATH)
+        P, I64 = ctypes.c_void_p, ctypes.c_int64
+        for name in ("fa_fwd", "fa_fwd_fp16"):
+            fn = getattr(L, name)
+            fn.argtypes = [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int, ctypes.c_float, P]
+            fn.restype = ctypes.c_int
+        L.fa_get_status.argtypes = [P]
+        L.fa_get_status.restype = ctypes.c_int
+        L.fa_strerror.argtypes = [ctypes.c_int]
+        L.fa_strerror.restype = ctypes.c_char_p
+        L.fa_last_cuda_error.argtypes = []
+        L.fa_last_cuda_error.restype = ctypes.c_int
+        L.fa_version.argtypes = []
+        L.fa_version.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def fa_strerror(code: int) -> str:
+    return lib().fa_strerror(int(code)).decode()
+
+
+def fa_version() -> int:
+    return lib().fa_version()
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(t, name, dtype, shape):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _call(fn_name, q, k, v, o, lse, causal, scale, stream, dtype):
+    import torch
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _check(t, name, dtype, (B, H, N, d))
+    _check(lse, "lse", torch.float32, (B, H, N))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc = getattr(lib(), fn_name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
+                                 _stream_handle(stream, q.device))
+    if rc != FA_OK:
+        raise FaError(rc, fn_name)
+
+
+def fa_fwd(q, k, v, o, lse, causal=False, scale=None, stream=None) -> None:
+    """bf16 attention forward into caller-provided o [B,H,N,d] and lse [B,H,N] fp32."""
+    import torch
+    _call("fa_fwd", q, k, v, o, lse, causal, scale, stream, torch.bfloat16)
+
+
+def fa_fwd_fp16(q, k, v, o, lse, causal=False, scale=None, stream=None) -> None:
+    """fp16 attention forward into caller-provided o and lse."""
+    import torch
+    _call("fa_fwd_fp16", q, k, v, o, lse, causal, scale, stream, torch.float16)
+
+
+def fa_get_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    import torch
+    return lib().fa_get_status(_stream_handle(stream, torch.cuda.current_device()))
+
+
+def forward(q, k, v, causal=False, scale=None, stream=None):
+    """Allocate o and lse with torch and run the forward; returns (o, lse)."""
+    import torch
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    if q.dtype == torch.bfloat16:
+        fa_fwd(q, k, v, o, lse, causal, scale, stream)
+    elif q.dtype == torch.float16:
+        fa_fwd_fp16(q, k, v, o, lse, causal, scale, stream)
+    else:
+        raise TypeError(f"unsupported dtype {q.dtype}: use bfloat16 or float16")
+    return o, lse

@@ -1,0 +1,247 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument checks, TMA
+// tensor-map encoding, per-device state and the kernel launch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_kernel.cuh"
+
+namespace {
+
+__device__ unsigned g_fa_status = 0;  // per-device status word (FA_ERR_TIMEOUT source)
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  std::once_flag once;
+  int err = FA_OK;  // FA_ERR_DEVICE / FA_ERR_CUDA if the device is unusable
+  int sm_count = 0;
+  unsigned *status = nullptr;  // device address of g_fa_status
+  std::once_flag attr_once[4];
+  int attr_err[4] = {0, 0, 0, 0};
+};
+
+DeviceState g_dev[kMaxDevices];
+thread_local int t_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return FA_ERR_CUDA;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Device checks once per device: compute capability 10.3 (the kernels are
+// built for sm_103a only), SM count, address of the status word.
+int device_state(DeviceState **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
+  DeviceState &s = g_dev[dev];
+  std::call_once(s.once, [&] {
+    int major = 0, minor = 0;
+    cudaError_t e1 = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaError_t e2 = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaError_t e3 = cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) {
+      t_last_cuda_error = static_cast<int>(e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3));
+      s.err = FA_ERR_CUDA;
+      return;
+    }
+    if (major != 10 || minor != 3) {
+      s.err = FA_ERR_DEVICE;
+      return;
+    }
+    void *addr = nullptr;
+    cudaError_t e4 = cudaGetSymbolAddress(&addr, g_fa_status);
+    if (e4 != cudaSuccess) {
+      t_last_cuda_error = static_cast<int>(e4);
+      s.err = FA_ERR_CUDA;
+      return;
+    }
+    s.status = static_cast<unsigned *>(addr);
+  });
+  if (s.err != FA_OK) return s.err;
+  *out = &s;
+  return FA_OK;
+}
+
+// [B*H, N, d] view, box 128 rows x 64 columns, 128-byte swizzle; rows past
+// N inside a box read as zero.
+int make_map(CUtensorMap *m, const void *base, bool bf16, int64_t BH, int64_t N, int64_t d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return FA_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2), static_cast<cuuint64_t>(N * d * 2)};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                  const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    t_last_cuda_error = static_cast<int>(r);
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+template <int D, bool BF16>
+int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *v, void *o,
+           float *lse, int64_t BH, int64_t N, int causal, float scale, cudaStream_t stream) {
+  using C = fa::Cfg<D, BF16>;
+  auto kernel = fa::fa_fwd_kernel<D, BF16>;
+  std::call_once(ds.attr_once[slot], [&] {
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    ds.attr_err[slot] = static_cast<int>(e);
+  });
+  if (ds.attr_err[slot] != 0) return cuda_fail(static_cast<cudaError_t>(ds.attr_err[slot]));
+
+  CUtensorMap tq, tk, tv;
+  int rc;
+  if ((rc = make_map(&tq, q, BF16, BH, N, D)) != FA_OK) return rc;
+  if ((rc = make_map(&tk, k, BF16, BH, N, D)) != FA_OK) return rc;
+  if ((rc = make_map(&tv, v, BF16, BH, N, D)) != FA_OK) return rc;
+
+  fa::Params p;
+  p.o = o;
+  p.lse = lse;
+  p.status = ds.status;
+  p.N = static_cast<int>(N);
+  p.BH = static_cast<int>(BH);
+  p.n_qtiles = static_cast<int>((N + 127) / 128);
+  p.n_pairs = (p.n_qtiles + 1) / 2;
+  p.n_items = p.BH * p.n_pairs;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.rescale_thr = 0.f;
+
+  const int grid = p.n_items < ds.sm_count ? p.n_items : ds.sm_count;
+  kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
+      return FA_ERR_DEVICE;
+    return cuda_fail(e);
+  }
+  return FA_OK;
+}
+
+int fwd_common(bool bf16, const void *q, const void *k, const void *v, void *o, float *lse,
+               int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
+               fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (N > FA_MAX_N) return FA_ERR_UNSUPPORTED_N;
+  // B*H*N*d elements (and the work-item count) must stay in range.
+  const int64_t kLimit = int64_t(1) << 40;
+  if (B > kLimit / H || B * H > kLimit / N || B * H * N > kLimit / d) return FA_ERR_SHAPE;
+  const int64_t BH = B * H;
+  if (BH * ((N + 255) / 256) > INT32_MAX / 2) return FA_ERR_SHAPE;
+  for (const void *ptr : {q, k, v, static_cast<const void *>(o)})
+    if (reinterpret_cast<uintptr_t>(ptr) & 15u) return FA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_ALIGN;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+  const size_t tbytes = static_cast<size_t>(BH * N * d) * 2;
+  const size_t lbytes = static_cast<size_t>(BH * N) * 4;
+  for (const void *in : {q, k, v})
+    if (overlaps(o, tbytes, in, tbytes) || overlaps(lse, lbytes, in, tbytes)) return FA_ERR_ALIAS;
+  if (overlaps(o, tbytes, lse, lbytes)) return FA_ERR_ALIAS;
+
+  DeviceState *ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != FA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (d == 64)
+    return bf16 ? launch<64, true>(*ds, 0, q, k, v, o, lse, BH, N, causal, scale, st)
+                : launch<64, false>(*ds, 1, q, k, v, o, lse, BH, N, causal, scale, st);
+  return bf16 ? launch<128, true>(*ds, 2, q, k, v, o, lse, BH, N, causal, scale, st)
+              : launch<128, false>(*ds, 3, q, k, v, o, lse, BH, N, causal, scale, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+           int64_t H, int64_t N, int64_t d, int causal, float scale, fa_stream_t stream) {
+  return fwd_common(true, q, k, v, o, lse, B, H, N, d, causal, scale, stream);
+}
+
+int fa_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                int64_t H, int64_t N, int64_t d, int causal, float scale,
+                fa_stream_t stream) {
+  return fwd_common(false, q, k, v, o, lse, B, H, N, d, causal, scale, stream);
+}
+
+int fa_get_status(fa_stream_t stream) {
+  DeviceState *ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != FA_OK) return rc;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned v = 0;
+  e = cudaMemcpy(&v, ds->status, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (v != 0) {
+    e = cudaMemset(ds->status, 0, sizeof(unsigned));
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return (v & fa::kStatusTimeout) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+const char *fa_strerror(int code) {
+  switch (code) {
+    case FA_OK: return "success";
+    case FA_ERR_NULL: return "a required pointer is NULL";
+    case FA_ERR_SHAPE: return "B, H and N must be >= 1 and B*H*N*d must fit the index range";
+    case FA_ERR_HEADDIM: return "head dimension d must be 64 or 128";
+    case FA_ERR_UNSUPPORTED_N: return "sequence length N exceeds FA_MAX_N";
+    case FA_ERR_ALIGN: return "q, k, v and o must be 16-byte aligned, lse 4-byte aligned";
+    case FA_ERR_SCALE: return "scale must be finite and > 0";
+    case FA_ERR_DEVICE: return "current device is not a compute capability 10.3 (sm_103a) GPU";
+    case FA_ERR_CUDA: return "a CUDA runtime or driver call failed (see fa_last_cuda_error)";
+    case FA_ERR_TIMEOUT: return "a pipeline wait inside the kernel gave up; outputs undefined";
+    case FA_ERR_ALIAS: return "an output buffer overlaps an input or the other output";
+    default: return "unknown error code";
+  }
+}
+
+int fa_last_cuda_error(void) { return t_last_cuda_error; }
+
+int fa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,502 @@
+// fa_kernel.cuh -- the attention forward kernel for sm_103a.
+//
+// One persistent CTA per SM walks a list of work items.  An item is a pair
+// of 128-row Q tiles of one (batch, head): tile 0 = rows [256p, 256p+128),
+// tile 1 = the next 128 rows.  This is the query-block parallelism of the
+// FlashAttention v2 work-partitioning diagram (pseudo-code panel, "parallel
+// for batch, head, q_block"; core panel item 2: more CTAs along the
+// sequence) and its sliced-Q split (each softmax warp owns 32 Q rows; K/V
+// tiles are shared and no warp reduces another's output).
+//
+// Roles inside the CTA (FlashAttention v4 Blackwell pipeline diagram, the
+// producer / MMA / softmax lanes and the pseudo-code panel):
+//   warps 0-3  softmax group 0: online softmax of Q tile 0, its O rescale and
+//              its epilogue (O / l, logsumexp)
+//   warps 4-7  softmax group 1: the same for Q tile 1
+//   warp  8    MMA issue (one thread) + tensor-memory allocation
+//   warp  9    TMA producer (one thread): Q tiles and a K/V ring
+//
+// Tensor memory (512 columns x 128 lanes, 32-bit cells):
+//   S0 [0,128)   S1 [128,256)   O0 [256,256+D)   O1 [256+D,256+2D)
+// S_t = Q_t K_j^T (fp32).  After the softmax reads S_t it writes P_t as
+// packed 16-bit pairs over the first 64 columns of S_t, and the second MMA
+// takes P_t straight from tensor memory: S and P never leave the chip.
+//
+// MMA issue order per K/V block j (ping-pong between the two Q tiles, so one
+// group's softmax overlaps the other group's MMAs):
+//   PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
+// Each S_t commit also covers the PV_t issued before it, so a softmax group
+// that sees S_t(j+1) ready may rescale O_t (PV_t(j) is complete) and the
+// MMA does not issue PV_t(j+1) until that group signals P_t ready.
+//
+// Every wait is bounded: after kTimeoutNs without progress the thread sets
+// the CTA's abort flag and the device status word, and all roles leave
+// their loops; in-flight copies and MMAs are drained before the tensor
+// memory is freed, so the context stays usable.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace fa {
+
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s without progress
+constexpr uint32_t kStatusTimeout = 1u;
+
+struct Params {
+  void *o;           // [BH, N, D] 16-bit
+  float *lse;        // [BH, N] fp32
+  unsigned *status;  // device status word
+  int N;             // sequence length
+  int BH;            // B * H
+  int n_qtiles;      // ceil(N / 128)
+  int n_pairs;       // ceil(n_qtiles / 2)
+  int n_items;       // BH * n_pairs
+  int causal;
+  float scale_log2;  // scale * log2(e)
+  float rescale_thr; // rescale O only when the running max grows by more than this (log2 units)
+};
+
+template <int D, bool BF16>
+struct Cfg {
+  static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
+  static constexpr int kRows = 128;                   // Q rows per tile, keys per block
+  static constexpr int kTileBytes = kRows * D * 2;    // one Q, K or V tile
+  static constexpr int kHalfBytes = kRows * 64 * 2;   // 64 columns: one 128-byte swizzle span
+  static constexpr int kStages = (D == 128) ? 4 : 8;  // K/V ring slots
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+  // barrier indices
+  static constexpr int kQFull = 0, kQEmpty = 1, kKVFull = 2, kKVEmpty = 2 + kStages;
+  static constexpr int kSFull = 2 + 2 * kStages, kPFull = kSFull + 2, kOFull = kPFull + 2;
+  static constexpr int kDrain = kOFull + 2;
+  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
+  static constexpr uint32_t kTmemCols = 512;
+  // tensor-memory column of S_t and O_t for Q tile t
+  static __device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
+  static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + D * t; }
+  static constexpr uint32_t kIdescS = idesc_f16(BF16, false, 128, 128);
+  static constexpr uint32_t kIdescO = idesc_f16(BF16, true, 128, D);
+  static constexpr int kThreads = 320;
+};
+
+struct Item {
+  int bh, qt0, n0, n1;
+};
+
+// Work item -> (head, first Q tile, K/V blocks for each of the two tiles).
+// Non-causal items run head-major so CTAs working at the same time share a
+// few heads' K/V in L2.  Causal items run heaviest pair first (the pair
+// nearest the end of the sequence sees the most keys).
+__device__ __forceinline__ Item decode_item(int item, const Params &p) {
+  Item it;
+  int pair;
+  if (p.causal) {
+    const int level = item / p.BH;
+    it.bh = item - level * p.BH;
+    pair = p.n_pairs - 1 - level;
+  } else {
+    it.bh = item / p.n_pairs;
+    pair = item - it.bh * p.n_pairs;
+  }
+  it.qt0 = 2 * pair;
+  const int qt1 = it.qt0 + 1;
+  it.n0 = p.causal ? it.qt0 + 1 : p.n_qtiles;
+  it.n1 = (qt1 < p.n_qtiles) ? (p.causal ? qt1 + 1 : p.n_qtiles) : 0;
+  return it;
+}
+
+// The item a CTA takes in a given round of the persistent loop, or -1.
+// Causal rounds alternate direction so the CTA that took the heaviest item
+// of one round takes the lightest of the next.
+__device__ __forceinline__ int round_item(int round, const Params &p) {
+  const int base = round * static_cast<int>(gridDim.x);
+  const int off = (p.causal && (round & 1)) ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
+                                            : static_cast<int>(blockIdx.x);
+  const int idx = base + off;
+  return idx < p.n_items ? idx : -1;
+}
+
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                       unsigned *status) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        atomicOr(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait for phase `parity` of barrier `bar`; false = give up.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         unsigned *status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, abort_flag, status);
+}
+
+// Drain wait: bounded by time only (the awaited copy or MMA needs nothing
+// from other threads to finish).
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kTimeoutNs) return;
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+  }
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(320, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  using C = Cfg<D, BF16>;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte-swizzled tiles.
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (sbase - raw);
+
+  const uint32_t bars = sbase + C::kBarOff;
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+  uint32_t *tmem_base_slot = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31u;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(bar(C::kKVFull + i), 1);
+      mbar_init(bar(C::kKVEmpty + i), 1);
+    }
+    mbar_init(bar(C::kQFull), 1);
+    mbar_init(bar(C::kQEmpty), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::kSFull + t), 1);
+      mbar_init(bar(C::kPFull + t), 4);  // one arrive per softmax warp
+      mbar_init(bar(C::kOFull + t), 1);
+    }
+    mbar_init(bar(C::kDrain), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  if (warp == 8) {
+    tmem_alloc(smem_u32(tmem_base_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_slot;
+
+  if (warp == 9) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_q = l2_policy_evict_first();
+      const uint64_t pol_kv = l2_policy_evict_last();
+      uint32_t slot = 0, phase = 0, q_phase = 0;
+      uint32_t kv_loads = 0, q_loads = 0;
+      bool ok = true;
+      for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_items; ++round) {
+        const int item = round_item(round, p);
+        if (item < 0) continue;
+        const Item it = decode_item(item, p);
+        if (!(ok = wait_bar(bar(C::kQEmpty), q_phase ^ 1u, abort_flag, p.status))) break;
+        q_phase ^= 1u;
+        const int nq = it.n1 > 0 ? 2 : 1;
+        mbar_arrive_expect_tx(bar(C::kQFull), nq * C::kTileBytes);
+        for (int t = 0; t < nq; ++t)
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(sbase + C::kQOff + t * C::kTileBytes + h * C::kHalfBytes, &tm_q,
+                        bar(C::kQFull), h * 64, (it.qt0 + t) * 128, it.bh, pol_q);
+        ++q_loads;
+        const int n_max = it.n0 > it.n1 ? it.n0 : it.n1;
+        for (int j = 0; ok && j < n_max; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {
+            if (!(ok = wait_bar(bar(C::kKVEmpty + slot), phase ^ 1u, abort_flag, p.status))) break;
+            mbar_arrive_expect_tx(bar(C::kKVFull + slot), C::kTileBytes);
+            const CUtensorMap *m = kv ? &tm_v : &tm_k;
+            for (int h = 0; h < D / 64; ++h)
+              tma_load_3d(sbase + C::kKVOff + slot * C::kTileBytes + h * C::kHalfBytes, m,
+                          bar(C::kKVFull + slot), h * 64, j * 128, it.bh, pol_kv);
+            ++kv_loads;
+            if (++slot == C::kStages) {
+              slot = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      // Drain: every issued copy must land before the CTA's shared memory
+      // can be released.  Slot s received loads s, s+S, s+2S, ... < kv_loads.
+      for (int s = 0; s < C::kStages; ++s) {
+        if (static_cast<uint32_t>(s) < kv_loads) {
+          const uint32_t cnt = (kv_loads - s + C::kStages - 1) / C::kStages;
+          wait_drain(bar(C::kKVFull + s), (cnt - 1) & 1u);
+        }
+      }
+      if (q_loads) wait_drain(bar(C::kQFull), (q_loads - 1) & 1u);
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      uint32_t slot = 0, phase = 0, q_phase = 0, p_phase[2] = {0, 0};
+      bool ok = true;
+      auto advance = [&]() {
+        if (++slot == C::kStages) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      };
+      auto issue_s = [&](int t, uint32_t kslot) {
+        const uint32_t q_addr = sbase + C::kQOff + t * C::kTileBytes;
+        const uint32_t k_addr = sbase + C::kKVOff + kslot * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+          mma_ss(tmem + C::col_s(t), smem_desc_sw128(q_addr + off, 16, 1024),
+                 smem_desc_sw128(k_addr + off, 16, 1024), C::kIdescS, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
+        const uint32_t v_addr = sbase + C::kKVOff + vslot * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 128 / 16; ++kk) {
+          mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
+                 smem_desc_sw128(v_addr + kk * 2048, C::kHalfBytes, 1024), C::kIdescO,
+                 (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_items; ++round) {
+        const int item = round_item(round, p);
+        if (item < 0) continue;
+        const Item it = decode_item(item, p);
+        const int n_max = it.n0 > it.n1 ? it.n0 : it.n1;
+        if (!(ok = wait_bar(bar(C::kQFull), q_phase, abort_flag, p.status))) break;
+        q_phase ^= 1u;
+        // K_0 and V_0 positions in the ring
+        uint32_t ks = slot, kph = phase;
+        advance();
+        uint32_t vs = slot, vph = phase;
+        advance();
+        if (!(ok = wait_bar(bar(C::kKVFull + ks), kph, abort_flag, p.status))) break;
+        tc_fence_after();
+        issue_s(0, ks);
+        mma_commit(bar(C::kSFull + 0));
+        if (it.n1 > 0) {
+          issue_s(1, ks);
+          mma_commit(bar(C::kSFull + 1));
+        }
+        mma_commit(bar(C::kKVEmpty + ks));
+        if (n_max == 1) mma_commit(bar(C::kQEmpty));
+        for (int j = 0; j < n_max; ++j) {
+          if (!(ok = wait_bar(bar(C::kKVFull + vs), vph, abort_flag, p.status))) break;
+          const bool more = j + 1 < n_max;
+          if (more) {
+            ks = slot;
+            kph = phase;
+            advance();
+          }
+          // tile 0
+          if (j < it.n0) {
+            if (!(ok = wait_bar(bar(C::kPFull + 0), p_phase[0], abort_flag, p.status))) break;
+            p_phase[0] ^= 1u;
+            tc_fence_after();
+            issue_pv(0, vs, j > 0);
+          }
+          if (more) {
+            if (!(ok = wait_bar(bar(C::kKVFull + ks), kph, abort_flag, p.status))) break;
+            tc_fence_after();
+          }
+          if (j + 1 < it.n0) {
+            issue_s(0, ks);
+            mma_commit(bar(C::kSFull + 0));
+          } else if (j + 1 == it.n0) {
+            mma_commit(bar(C::kOFull + 0));
+          }
+          // tile 1
+          if (j < it.n1) {
+            if (!(ok = wait_bar(bar(C::kPFull + 1), p_phase[1], abort_flag, p.status))) break;
+            p_phase[1] ^= 1u;
+            tc_fence_after();
+            issue_pv(1, vs, j > 0);
+          }
+          mma_commit(bar(C::kKVEmpty + vs));
+          if (j + 1 < it.n1) {
+            issue_s(1, ks);
+            mma_commit(bar(C::kSFull + 1));
+          } else if (j + 1 == it.n1) {
+            mma_commit(bar(C::kOFull + 1));
+          }
+          if (more) {
+            mma_commit(bar(C::kKVEmpty + ks));
+            if (j + 2 == n_max) mma_commit(bar(C::kQEmpty));
+            vs = slot;
+            vph = phase;
+            advance();
+          }
+        }
+      }
+      // Drain: all issued MMAs complete before tensor memory is freed.
+      mma_commit(bar(C::kDrain));
+      wait_drain(bar(C::kDrain), 0);
+    }
+  } else {
+    // ---------------------------------------------------- softmax groups
+    const int t = warp >> 2;                      // Q tile of this group
+    const uint32_t lane_base = (warp & 3) * 32u;  // this warp's TMEM lane quadrant
+    const int row = static_cast<int>(lane_base + lane);
+    const uint32_t t_lane = tmem + (lane_base << 16);
+    const uint32_t tS = t_lane + C::col_s(t);
+    const uint32_t tO = t_lane + C::col_o(t);
+    const float sl2 = p.scale_log2;
+    uint32_t s_phase = 0, o_phase = 0;
+    bool ok = true;
+    for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_items; ++round) {
+      const int item = round_item(round, p);
+      if (item < 0) continue;
+      const Item it = decode_item(item, p);
+      const int n = t ? it.n1 : it.n0;
+      if (n == 0) continue;
+      const int qt = it.qt0 + t;
+      const int q_idx = qt * 128 + row;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < n; ++j) {
+        ok = wait_bar(bar(C::kSFull + t), s_phase, abort_flag, p.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        s_phase ^= 1u;
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+        float s[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+        // mask only where needed: the diagonal block (causal) or the ragged
+        // last block (non-causal, N % 128 != 0)
+        if (p.causal && j == qt) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > row) s[c] = -INFINITY;
+        } else if (!p.causal && j == p.n_qtiles - 1 && (p.N & 127)) {
+          const int lim = p.N - j * 128;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) s[c] = -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx[u] = s[u];
+#pragma unroll
+        for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+        const float rmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float m_cand = fmaxf(m, rmax * sl2);
+        const bool need = (m_cand - m) > p.rescale_thr;
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2_approx(m - m_cand);
+          m = m_cand;
+        }
+        const float neg_m = -m;
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[2][32];
+#pragma unroll
+        for (int c = 0; c < 128; c += 2) {
+          const float p0 = ex2_approx(fmaf(s[c], sl2, neg_m));
+          const float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg_m));
+          sum[(c >> 1) & 3] += p0 + p1;
+          pk[c >> 6][(c >> 1) & 31] = pack2<BF16>(p0, p1);
+        }
+        tmem_st32(tS + 0, pk[0]);
+        tmem_st32(tS + 32, pk[1]);
+        l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+        // Conditional rescale of the running output (v4 pseudo-code panel:
+        // "if need_rescale(m, m_new): acc *= exp(m - m_new)"), done once the
+        // S values are no longer live.  PV(j-1) is complete: its commit
+        // precedes this block's S commit; PV(j) waits for this group's signal.
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t orr[32];
+            tmem_ld32(tO + 32 * c, orr);
+            tmem_ld_wait(orr);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) orr[u] = __float_as_uint(__uint_as_float(orr[u]) * alpha);
+            tmem_st32(tO + 32 * c, orr);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::kPFull + t));
+      }
+      if (!ok) break;
+      // ------------------------------------------------------ epilogue
+      ok = wait_bar(bar(C::kOFull + t), o_phase, abort_flag, p.status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      o_phase ^= 1u;
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const bool live = q_idx < p.N;
+      const size_t row_off = (static_cast<size_t>(it.bh) * p.N + q_idx);
+      uint4 *orow = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + row_off * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t orr[32];
+        tmem_ld32(tO + 32 * c, orr);
+        tmem_ld_wait(orr);
+        uint32_t pk16[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          pk16[u] = pack2<BF16>(__uint_as_float(orr[2 * u]) * inv_l,
+                                __uint_as_float(orr[2 * u + 1]) * inv_l);
+        if (live) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            orow[c * 4 + u] = make_uint4(pk16[4 * u], pk16[4 * u + 1], pk16[4 * u + 2],
+                                         pk16[4 * u + 3]);
+        }
+      }
+      if (live) p.lse[row_off] = (m + lg2_approx(l)) * 0.6931471805599453f;
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace fa

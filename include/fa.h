@@ -1,0 +1,105 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact attention forward library.
+ *
+ * The operation (FlashAttention v4 Blackwell pipeline diagram, pseudo-code
+ * panel; FlashAttention v2 work-partitioning diagram, pseudo-code panel; the
+ * "flash attention v2 论文" search page, which states the result is exact
+ * attention, not an approximation):
+ *
+ *   O[b,h,i,:] = sum_{j in A(i)} softmax_j(scale * <Q[b,h,i,:], K[b,h,j,:]>) V[b,h,j,:]
+ *   LSE[b,h,i] = ln sum_{j in A(i)} exp(scale * <Q[b,h,i,:], K[b,h,j,:]>)
+ *
+ * with A(i) = {0..N-1}, or {0..i} when causal.  The scores S and the
+ * probabilities P are computed tile by tile on chip with the online-softmax
+ * recurrence and never written to memory.
+ *
+ * Layout (all entry points): q, k, v, o are dense, contiguous, row-major
+ * [B, H, N, d] arrays of 16-bit elements; element (b,h,n,c) is at index
+ * ((b*H + h)*N + n)*d + c.  lse is a dense [B, H, N] fp32 array.  Q, K and V
+ * share N (self-attention shape).  Every pointer is a DEVICE pointer on the
+ * current CUDA device.
+ *
+ * Ownership: the caller allocates and owns every buffer; the library
+ * allocates nothing per call.  Per-device state (SM count, kernel
+ * attributes, one 4-byte status word) is created on first use and lives
+ * until process exit.  o and lse must not overlap q, k, v or each other.
+ *
+ * Execution: asynchronous on `stream` (0 = legacy default stream); no host
+ * synchronisation.  Safe to call from several host threads.
+ *
+ * Errors: 0 on success, a negative FA_ERR_* code otherwise.  On an argument
+ * error nothing is launched and o/lse are not written.  Faults seen while
+ * the kernel runs (a pipeline wait that gave up) are recorded in the
+ * device status word and returned by fa_get_status().
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, passed as an opaque pointer so this header needs no CUDA
+ * headers. */
+typedef void *fa_stream_t;
+
+#define FA_OK 0
+#define FA_ERR_NULL (-1)           /* a required pointer is NULL */
+#define FA_ERR_SHAPE (-2)          /* B, H or N < 1, or B*H*N*d overflows */
+#define FA_ERR_HEADDIM (-3)        /* d is not 64 or 128 */
+#define FA_ERR_UNSUPPORTED_N (-4)  /* N above FA_MAX_N */
+#define FA_ERR_ALIGN (-5)          /* a pointer is not 16-byte aligned */
+#define FA_ERR_SCALE (-6)          /* scale is not finite and > 0 */
+#define FA_ERR_DEVICE (-7)         /* current device is not compute capability 10.3 */
+#define FA_ERR_CUDA (-8)           /* a CUDA runtime/driver call failed */
+#define FA_ERR_TIMEOUT (-9)        /* a pipeline wait inside the kernel gave up */
+#define FA_ERR_ALIAS (-10)         /* an output overlaps an input or the other output */
+
+#define FA_MAX_N (1 << 20)         /* longest sequence accepted */
+
+/*
+ * fa_fwd -- attention forward on bf16 inputs.
+ *   q, k, v : [B,H,N,d] bf16, read only
+ *   o       : [B,H,N,d] bf16, written (softmax-weighted sum of V rows,
+ *             fp32 accumulation, rounded to nearest even)
+ *   lse     : [B,H,N] fp32, written (natural-log logsumexp of the scaled
+ *             logits over the visible keys)
+ *   d       : 64 or 128
+ *   causal  : nonzero => query i sees keys 0..i only (top-left aligned)
+ *   scale   : multiplies Q K^T before the mask and softmax; finite, > 0
+ *             (usually 1/sqrt(d))
+ *   stream  : cudaStream_t to launch on
+ */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+           int64_t H, int64_t N, int64_t d, int causal, float scale, fa_stream_t stream);
+
+/* fa_fwd_fp16 -- identical to fa_fwd with fp16 q, k, v and o. */
+int fa_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                int64_t H, int64_t N, int64_t d, int causal, float scale,
+                fa_stream_t stream);
+
+/*
+ * fa_get_status -- synchronises `stream`, then returns and clears the
+ * current device's status word: FA_OK, or FA_ERR_TIMEOUT if some launch
+ * since the last call had a pipeline wait give up (its outputs are then
+ * undefined).  FA_ERR_CUDA if the synchronisation itself failed.
+ */
+int fa_get_status(fa_stream_t stream);
+
+/* fa_strerror -- static, human-readable text for a FA_* code. */
+const char *fa_strerror(int code);
+
+/* fa_last_cuda_error -- the cudaError_t behind the calling thread's most
+ * recent FA_ERR_CUDA (0 if none). */
+int fa_last_cuda_error(void);
+
+/* fa_version -- library version, major*10000 + minor*100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

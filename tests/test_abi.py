@@ -1,0 +1,87 @@
+"""The C-ABI library loads, exports every function include/fa.h declares,
+and rejects bad arguments before touching the GPU (no launch, no device
+call: runs on a machine without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_forward_07_gb300 as fa
+from exact_attention_forward_07_gb300 import build as fa_build
+
+HEADER = os.path.join(fa_build.INCLUDE, "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return fa.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_fwd_fp16", "fa_get_status", "fa_strerror", "fa_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in fa.h but not exported"
+
+
+def test_version_and_strerror(lib):
+    assert lib.fa_version() == 100
+    for code in range(0, -11, -1):
+        msg = fa.fa_strerror(code)
+        assert msg and msg != "unknown error code"
+    assert fa.fa_strerror(-999) == "unknown error code"
+
+
+# Fake, 16-byte aligned, distinct "device" addresses: argument checks run
+# before any CUDA call, so nothing dereferences them.
+Q, K, V, O, L = 0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000
+
+
+def call(lib, q=Q, k=K, v=V, o=O, lse=L, B=1, H=1, N=128, d=64, causal=0, scale=0.125,
+         fp16=False):
+    fn = lib.fa_fwd_fp16 if fp16 else lib.fa_fwd
+    return fn(q, k, v, o, lse, B, H, N, d, causal, scale, None)
+
+
+@pytest.mark.parametrize("fp16", [False, True])
+def test_argument_errors(lib, fp16):
+    c = lambda **kw: call(lib, fp16=fp16, **kw)
+    assert c(q=None) == fa.FA_ERR_NULL
+    assert c(lse=None) == fa.FA_ERR_NULL
+    assert c(B=0) == fa.FA_ERR_SHAPE
+    assert c(H=-1) == fa.FA_ERR_SHAPE
+    assert c(N=0) == fa.FA_ERR_SHAPE
+    assert c(d=96) == fa.FA_ERR_HEADDIM
+    assert c(d=256) == fa.FA_ERR_HEADDIM
+    assert c(N=fa.FA_MAX_N + 1) == fa.FA_ERR_UNSUPPORTED_N
+    assert c(B=1 << 30, H=1 << 30) == fa.FA_ERR_SHAPE
+    assert c(q=Q + 8) == fa.FA_ERR_ALIGN
+    assert c(o=O + 2) == fa.FA_ERR_ALIGN
+    assert c(lse=L + 2) == fa.FA_ERR_ALIGN
+    assert c(scale=0.0) == fa.FA_ERR_SCALE
+    assert c(scale=-0.5) == fa.FA_ERR_SCALE
+    assert c(scale=float("inf")) == fa.FA_ERR_SCALE
+    assert c(scale=float("nan")) == fa.FA_ERR_SCALE
+    assert c(o=Q) == fa.FA_ERR_ALIAS
+    assert c(o=K + 64) == fa.FA_ERR_ALIAS
+    assert c(lse=V) == fa.FA_ERR_ALIAS
+    assert c(lse=O + 128) == fa.FA_ERR_ALIAS
+
+
+def test_python_binding_rejects_cpu_tensors(lib):
+    import torch
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q, q, q, q.clone(), torch.zeros(1, 1, 128))
