@@ -1,0 +1,418 @@
+"""Throughput benchmark of the attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+A step is one forward (O and LSE) over the whole workload; by default the
+bf16 d=128, N=4096 batch [B=8, H=16, N=4096, d=128], non-causal, seeded
+N(0,1) inputs.  Prints one JSON line (rank 0).  The metric is TFLOPS with
+4*B*H*N^2*d FLOPs per step (halved when causal).
+
+Timing: W warm-up steps, then exactly K steps between a barrier and a
+device synchronisation on both sides, timed with CUDA events on the stream
+the kernel is launched on; the maximum over ranks is reported.  Q+K+V
+(384 MiB for the default) exceed the 126 MB L2, so no flush is needed
+between steps.  Under torchrun each rank runs the same workload on its own
+GPU (heads are independent: weak scaling, no data-path collective).
+
+`e2e` repeats the measurement through the public API with pinned host
+buffers: every step copies Q, K, V host->device, runs the forward and
+copies O and LSE back, all inside the timed region.
+
+`--impl reference` times the CPU oracle (the reference arm: a plain fp64
+C implementation of the definition) on the host cores, each step a bounded
+sample of the same workload (128 query rows of one head).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from attn_inputs import WORKLOADS, make_workload_inputs  # noqa: E402
+
+METRIC = "attention fwd TFLOPS (bf16, 1×GB300) and fraction of dense tensor-core peak"
+DEFAULT_WORKLOAD = "b8h16n4096d128"
+FALLBACK_BF16_TFLOPS = 1900.0
+KERNEL_SOURCES = ["fa_api.cu", "fa_kernel.cuh", "ptx.cuh"]
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "fa_fwd_kernel_b8h16n4096d128.md")
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "exact_attention_forward_07_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, or None when
+    the kernel sources changed since that capture."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    m_traffic = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not (m_hash and m_traffic) or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_traffic.group(1))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.out_path = os.path.join("/tmp", f"fa_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.out_path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.out_path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.out_path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        busy = [s for s in sm if smax and s >= 0.3 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+L2_BYTES = 126 * 1024 * 1024
+
+
+def l2_note(w) -> str:
+    qkv = 3 * w.B * w.H * w.N * w.d * 2
+    if qkv > L2_BYTES:
+        return f"no flush: Q+K+V ({qkv / 2**20:.0f} MiB) exceed the 126 MB L2"
+    return (f"L2-resident: Q+K+V ({qkv / 2**20:.1f} MiB) fit in L2 and are not flushed "
+            "between steps")
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def oracle_sample(w, q, k, v, n_heads: int, rows_per_head=None):
+    """Time the oracle on a bounded sample: all (or `rows_per_head`) query
+    rows of `n_heads` heads.  Returns (TFLOPS, seconds, description)."""
+    import numpy as np
+    import oracle
+    BH = w.B * w.H
+    heads = list(range(min(n_heads, BH)))
+    sub = [x.reshape(BH, 1, w.N, w.d)[heads].reshape(1, len(heads), w.N, w.d) for x in (q, k, v)]
+    if rows_per_head is None:
+        rows = np.arange(len(heads) * w.N, dtype=np.int64)
+    else:
+        rows = np.concatenate([h * w.N + np.arange(rows_per_head[0], rows_per_head[1])
+                               for h in range(len(heads))]).astype(np.int64)
+    i = rows % w.N
+    keys = (i + 1) if w.causal else np.full_like(i, w.N)
+    flops = float(np.sum(4.0 * keys * w.d))
+    sub64 = [oracle._as_f64(x) for x in sub]  # upcast outside the timed region
+    t0 = time.perf_counter()
+    oracle.attn_fwd(*sub64, w.causal, w.scale, rows=rows, nthreads=cpu_cores())
+    dt = time.perf_counter() - t0
+    desc = (f"{len(rows)} query rows ({len(heads)} head(s) x "
+            f"{'all' if rows_per_head is None else rows_per_head[1] - rows_per_head[0]} rows) "
+            f"of {w.name}, fp64, {cpu_cores()} threads")
+    return flops / dt / 1e12, dt, desc
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    q, k, v = make_workload_inputs(w)
+    BH = w.B * w.H
+    tiles = (w.N + 127) // 128
+    oracle_sample_step(w, q, k, v, 0, BH, tiles)  # fp64 head copies, untimed
+    for i in range(args.warmup):
+        oracle_sample_step(w, q, k, v, i, BH, tiles)
+    flops = 0.0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flops += oracle_sample_step(w, q, k, v, args.warmup + i, BH, tiles)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(w.describe(), sample="128 query rows of one head per step"),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cpu_cores(),
+                         "kind": "oracle",
+                         "sample": f"each step: 128 consecutive query rows of one head of "
+                                   f"{w.name} (fp64 C oracle, {cpu_cores()} threads)"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+_ref_heads = {}
+
+
+def oracle_sample_step(w, q, k, v, i, BH, tiles):
+    """One reference step: 128 consecutive query rows of one head (cycling
+    over up to 8 heads whose fp64 copies are made before timing starts)."""
+    import numpy as np
+    import oracle
+    if not _ref_heads:
+        for h in range(min(8, BH)):
+            _ref_heads[h] = [oracle._as_f64(x.reshape(BH, 1, w.N, w.d)[h:h + 1].reshape(
+                1, 1, w.N, w.d)) for x in (q, k, v)]
+    sub = _ref_heads[i % len(_ref_heads)]
+    tile = (i * 3) % tiles
+    lo, hi = tile * 128, min(w.N, tile * 128 + 128)
+    rows = np.arange(lo, hi, dtype=np.int64)
+    keys = (rows + 1) if w.causal else np.full_like(rows, w.N)
+    oracle.attn_fwd(*sub, w.causal, w.scale, rows=rows, nthreads=cpu_cores())
+    return float(np.sum(4.0 * keys * w.d))
+
+
+def run_ours(args, w):
+    import torch
+
+    import exact_attention_forward_07_gb300 as fa
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    q_h, k_h, v_h = make_workload_inputs(w)
+    q, k, v = (x.to(dev) for x in (q_h, k_h, v_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    call = fa.fa_fwd if w.dtype == "bf16" else fa.fa_fwd_fp16
+    stream = torch.cuda.current_stream(dev)
+    flops = w.flops()
+
+    for _ in range(args.warmup):
+        call(q, k, v, o, lse, causal=w.causal, stream=stream)
+    torch.cuda.synchronize(dev)
+    status = fa.fa_get_status(stream)
+    if status != 0:
+        raise RuntimeError(f"kernel status {status}: {fa.fa_strerror(status)}")
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.25)
+    # ---------------------------------------------------------- timed region
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        call(q, k, v, o, lse, causal=w.causal, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    # ------------------------------------------------------------------------
+    clocks = sampler.stop()
+    ms_local = ev0.elapsed_time(ev1)
+    ms_total = max_over_ranks(ms_local, world)
+    ms_step = ms_total / args.steps
+    value = world * flops * args.steps / (ms_total * 1e-3) / 1e12
+    kernel_tflops = flops / (ms_local / args.steps * 1e-3) / 1e12
+    status = fa.fa_get_status(stream)
+    if status != 0:
+        raise RuntimeError(f"kernel status {status}: {fa.fa_strerror(status)}")
+
+    # ------------------------------------------------ end to end, host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = [x.pin_memory() for x in (q_h, k_h, v_h)]
+        o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        n_e2e = max(1, min(args.steps, args.e2e_steps))
+
+        def e2e_step():
+            q.copy_(pin[0], non_blocking=True)
+            k.copy_(pin[1], non_blocking=True)
+            v.copy_(pin[2], non_blocking=True)
+            call(q, k, v, o, lse, causal=w.causal, stream=stream)
+            o_h.copy_(o, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+
+        for _ in range(min(3, args.warmup) or 1):
+            e2e_step()
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+        h2d = sum(x.numel() * x.element_size() for x in pin)
+        d2h = o_h.numel() * o_h.element_size() + lse_h.numel() * lse_h.element_size()
+        e2e = {"value": world * flops * n_e2e / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "ms_per_step": e2e_ms / n_e2e}
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = measured_peaks()
+    roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peak,
+                "unit": "TFLOP/s", "frac": kernel_tflops / peak,
+                "peak_source": f"bf16_tflops burst, {peak_kind}",
+                "traffic": profiled_traffic(),
+                "kernel": "fa_fwd_kernel<%d,%s>" % (w.d, "bf16" if w.dtype == "bf16" else "fp16")}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        q64 = [q_h, k_h, v_h]
+        n_heads = max(1, int(args.cpu_heads))
+        tf, dt, desc = oracle_sample(w, *q64, n_heads=n_heads)
+        cpu = {"value": tf, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
+               "sample": desc, "seconds": dt}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": dict(w.describe(), parallelism=f"replicas{world}" if world > 1 else "single",
+                       l2=l2_note(w)),
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-heads", type=int, default=16)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    _, world, _ = dist_env()
+    if world != args.gpus:
+        if args.gpus != 1 or world != 1:
+            print(f"note: --gpus {args.gpus} but WORLD_SIZE={world}; using WORLD_SIZE",
+                  file=sys.stderr)
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
