@@ -16,7 +16,7 @@ import ctypes
 import math
 import os
 
-__all__ = ["FaError", "fa_fwd", "fa_fwd_fp16", "fa_get_status", "fa_strerror", "fa_version",
+__all__ = ["FaError", "fa_fwd", "fa_fwd_fp16", "fa_fwd_ex", "fa_get_status", "fa_strerror", "fa_version",
            "forward", "library_path", "lib"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -33,7 +33,10 @@ FA_ERR_DEVICE = -7
 FA_ERR_CUDA = -8
 FA_ERR_TIMEOUT = -9
 FA_ERR_ALIAS = -10
+FA_ERR_OPTION = -11
 FA_MAX_N = 1 << 20
+FA_DEFAULT_RESCALE_THRESHOLD = 8.0
+FA_MAX_RESCALE_THRESHOLD = 12.0
 
 _lib = None
 
@@ -65,6 +68,9 @@ def lib():
             fn = getattr(L, name)
             fn.argtypes = [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int, ctypes.c_float, P]
             fn.restype = ctypes.c_int
+        L.fa_fwd_ex.argtypes = [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int, ctypes.c_float,
+                                ctypes.c_int, ctypes.c_float, P]
+        L.fa_fwd_ex.restype = ctypes.c_int
         L.fa_get_status.argtypes = [P]
         L.fa_get_status.restype = ctypes.c_int
         L.fa_strerror.argtypes = [ctypes.c_int]
@@ -106,7 +112,7 @@ def _check(t, name, dtype, shape):
         raise ValueError(f"{name} must be contiguous")
 
 
-def _call(fn_name, q, k, v, o, lse, causal, scale, stream, dtype):
+def _call(fn_name, q, k, v, o, lse, causal, scale, stream, dtype, extra=()):
     import torch
     if q.dim() != 4:
         raise ValueError("q must be [B, H, N, d]")
@@ -118,7 +124,7 @@ def _call(fn_name, q, k, v, o, lse, causal, scale, stream, dtype):
         scale = 1.0 / math.sqrt(d)
     rc = getattr(lib(), fn_name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                  lse.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
-                                 _stream_handle(stream, q.device))
+                                 *extra, _stream_handle(stream, q.device))
     if rc != FA_OK:
         raise FaError(rc, fn_name)
 
@@ -135,18 +141,34 @@ def fa_fwd_fp16(q, k, v, o, lse, causal=False, scale=None, stream=None) -> None:
     _call("fa_fwd_fp16", q, k, v, o, lse, causal, scale, stream, torch.float16)
 
 
+def fa_fwd_ex(q, k, v, o, lse, causal=False, scale=None, rescale_threshold=None,
+              stream=None) -> None:
+    """Forward with an explicit online-softmax rescale threshold (log2 units;
+    0 = rescale whenever the running max grows).  dtype from q (bf16/fp16)."""
+    import torch
+    if rescale_threshold is None:
+        rescale_threshold = FA_DEFAULT_RESCALE_THRESHOLD
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"unsupported dtype {q.dtype}: use bfloat16 or float16")
+    fp16 = int(q.dtype == torch.float16)
+    _call("fa_fwd_ex", q, k, v, o, lse, causal, scale, stream, q.dtype,
+          extra=(fp16, float(rescale_threshold)))
+
+
 def fa_get_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status code."""
     import torch
     return lib().fa_get_status(_stream_handle(stream, torch.cuda.current_device()))
 
 
-def forward(q, k, v, causal=False, scale=None, stream=None):
+def forward(q, k, v, causal=False, scale=None, stream=None, rescale_threshold=None):
     """Allocate o and lse with torch and run the forward; returns (o, lse)."""
     import torch
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
-    if q.dtype == torch.bfloat16:
+    if rescale_threshold is not None:
+        fa_fwd_ex(q, k, v, o, lse, causal, scale, rescale_threshold, stream)
+    elif q.dtype == torch.bfloat16:
         fa_fwd(q, k, v, o, lse, causal, scale, stream)
     elif q.dtype == torch.float16:
         fa_fwd_fp16(q, k, v, o, lse, causal, scale, stream)

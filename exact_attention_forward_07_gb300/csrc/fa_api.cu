@@ -117,7 +117,8 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 
 template <int D, bool BF16>
 int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *v, void *o,
-           float *lse, int64_t BH, int64_t N, int causal, float scale, cudaStream_t stream) {
+           float *lse, int64_t BH, int64_t N, int causal, float scale, float thr,
+           cudaStream_t stream) {
   using C = fa::Cfg<D, BF16>;
   auto kernel = fa::fa_fwd_kernel<D, BF16>;
   std::call_once(ds.attr_once[slot], [&] {
@@ -144,7 +145,7 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
   p.n_items = p.BH * p.n_pairs;
   p.causal = causal ? 1 : 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  p.rescale_thr = 0.f;
+  p.rescale_thr = thr;
 
   const int grid = p.n_items < ds.sm_count ? p.n_items : ds.sm_count;
   kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
@@ -159,7 +160,7 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
 
 int fwd_common(bool bf16, const void *q, const void *k, const void *v, void *o, float *lse,
                int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
-               fa_stream_t stream) {
+               float thr, fa_stream_t stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_HEADDIM;
@@ -173,6 +174,7 @@ int fwd_common(bool bf16, const void *q, const void *k, const void *v, void *o, 
     if (reinterpret_cast<uintptr_t>(ptr) & 15u) return FA_ERR_ALIGN;
   if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_ALIGN;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+  if (!(thr >= 0.f && thr <= FA_MAX_RESCALE_THRESHOLD)) return FA_ERR_OPTION;
   const size_t tbytes = static_cast<size_t>(BH * N * d) * 2;
   const size_t lbytes = static_cast<size_t>(BH * N) * 4;
   for (const void *in : {q, k, v})
@@ -184,10 +186,10 @@ int fwd_common(bool bf16, const void *q, const void *k, const void *v, void *o, 
   if (rc != FA_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (d == 64)
-    return bf16 ? launch<64, true>(*ds, 0, q, k, v, o, lse, BH, N, causal, scale, st)
-                : launch<64, false>(*ds, 1, q, k, v, o, lse, BH, N, causal, scale, st);
-  return bf16 ? launch<128, true>(*ds, 2, q, k, v, o, lse, BH, N, causal, scale, st)
-              : launch<128, false>(*ds, 3, q, k, v, o, lse, BH, N, causal, scale, st);
+    return bf16 ? launch<64, true>(*ds, 0, q, k, v, o, lse, BH, N, causal, scale, thr, st)
+                : launch<64, false>(*ds, 1, q, k, v, o, lse, BH, N, causal, scale, thr, st);
+  return bf16 ? launch<128, true>(*ds, 2, q, k, v, o, lse, BH, N, causal, scale, thr, st)
+              : launch<128, false>(*ds, 3, q, k, v, o, lse, BH, N, causal, scale, thr, st);
 }
 
 }  // namespace
@@ -196,13 +198,22 @@ extern "C" {
 
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
            int64_t H, int64_t N, int64_t d, int causal, float scale, fa_stream_t stream) {
-  return fwd_common(true, q, k, v, o, lse, B, H, N, d, causal, scale, stream);
+  return fwd_common(true, q, k, v, o, lse, B, H, N, d, causal, scale,
+                    FA_DEFAULT_RESCALE_THRESHOLD, stream);
 }
 
 int fa_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
                 int64_t H, int64_t N, int64_t d, int causal, float scale,
                 fa_stream_t stream) {
-  return fwd_common(false, q, k, v, o, lse, B, H, N, d, causal, scale, stream);
+  return fwd_common(false, q, k, v, o, lse, B, H, N, d, causal, scale,
+                    FA_DEFAULT_RESCALE_THRESHOLD, stream);
+}
+
+int fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+              int64_t H, int64_t N, int64_t d, int causal, float scale, int fp16,
+              float rescale_threshold, fa_stream_t stream) {
+  return fwd_common(fp16 == 0, q, k, v, o, lse, B, H, N, d, causal, scale, rescale_threshold,
+                    stream);
 }
 
 int fa_get_status(fa_stream_t stream) {
@@ -236,6 +247,7 @@ const char *fa_strerror(int code) {
     case FA_ERR_CUDA: return "a CUDA runtime or driver call failed (see fa_last_cuda_error)";
     case FA_ERR_TIMEOUT: return "a pipeline wait inside the kernel gave up; outputs undefined";
     case FA_ERR_ALIAS: return "an output buffer overlaps an input or the other output";
+    case FA_ERR_OPTION: return "rescale_threshold must lie in [0, FA_MAX_RESCALE_THRESHOLD]";
     default: return "unknown error code";
   }
 }

@@ -15,6 +15,8 @@
 //   warps 4-7  softmax group 1: the same for Q tile 1
 //   warp  8    MMA issue (one thread) + tensor-memory allocation
 //   warp  9    TMA producer (one thread): Q tiles and a K/V ring
+//   warps 10-11 idle (they complete the third warpgroup, whose registers
+//              are handed to the softmax groups with setmaxnreg)
 //
 // Tensor memory (512 columns x 128 lanes, 32-bit cells):
 //   S0 [0,128)   S1 [128,256)   O0 [256,256+D)   O1 [256+D,256+2D)
@@ -82,7 +84,9 @@ struct Cfg {
   static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + D * t; }
   static constexpr uint32_t kIdescS = idesc_f16(BF16, false, 128, 128);
   static constexpr uint32_t kIdescO = idesc_f16(BF16, true, 128, D);
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 384;  // three warpgroups
+  // setmaxnreg split: 2 x 128 x 208 + 128 x 88 = 384 x 168 (the launch budget)
+  static constexpr uint32_t kRegsSoftmax = 208, kRegsOther = 88;
 };
 
 struct Item {
@@ -122,7 +126,7 @@ __device__ __forceinline__ int round_item(int round, const Params &p) {
   return idx < p.n_items ? idx : -1;
 }
 
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                        unsigned *status) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -165,8 +169,19 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// The two 16-bit values of a packed pair, widened back to fp32 (exact).
+template <bool BF16>
+__device__ __forceinline__ uint64_t unpack2(uint32_t v) {
+  if constexpr (BF16) {
+    return f2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+  } else {
+    __half2 h = *reinterpret_cast<__half2 *>(&v);
+    return f2(__low2float(h), __high2float(h));
+  }
+}
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
   using C = Cfg<D, BF16>;
@@ -214,7 +229,11 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_base_slot;
 
-  if (warp == 9) {
+  if (warp >= 8) {
+    // Each role's code sits under its own setmaxnreg, so the compiler sizes
+    // it for that role's register budget only.
+    regs_dec<C::kRegsOther>();
+    if (warp == 9) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol_q = l2_policy_evict_first();
@@ -262,7 +281,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (q_loads) wait_drain(bar(C::kQFull), (q_loads - 1) & 1u);
     }
-  } else if (warp == 8) {
+    } else if (warp == 8) {
     // ------------------------------------------------------------- MMA issue
     if (lane == 0) {
       uint32_t slot = 0, phase = 0, q_phase = 0, p_phase[2] = {0, 0};
@@ -366,7 +385,9 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit(bar(C::kDrain));
       wait_drain(bar(C::kDrain), 0);
     }
+    }
   } else {
+    regs_inc<C::kRegsSoftmax>();
     // ---------------------------------------------------- softmax groups
     const int t = warp >> 2;                      // Q tile of this group
     const uint32_t lane_base = (warp & 3) * 32u;  // this warp's TMEM lane quadrant
@@ -385,7 +406,7 @@ __global__ void __launch_bounds__(320, 1)
       if (n == 0) continue;
       const int qt = it.qt0 + t;
       const int q_idx = qt * 128 + row;
-      float m = -INFINITY, l = 0.f;
+      float m = -INFINITY, l = 0.f, lr = 0.f;  // max (log2 units), sums of P, of rounded P
       for (int j = 0; j < n; ++j) {
         ok = wait_bar(bar(C::kSFull + t), s_phase, abort_flag, p.status);
         ok = __all_sync(0xffffffffu, ok);
@@ -412,13 +433,18 @@ __global__ void __launch_bounds__(320, 1)
           for (int c = 0; c < 128; ++c)
             if (c >= lim) s[c] = -INFINITY;
         }
-        float mx[8];
+        // row max: three-input max over s[4..127] in four chains
+        float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mx[u] = s[u];
-#pragma unroll
-        for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-        const float rmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int c = 4; c < 124; c += 8) {
+          mx[0] = fmax3(mx[0], s[c], s[c + 1]);
+          mx[1] = fmax3(mx[1], s[c + 2], s[c + 3]);
+          mx[2] = fmax3(mx[2], s[c + 4], s[c + 5]);
+          mx[3] = fmax3(mx[3], s[c + 6], s[c + 7]);
+        }
+        mx[0] = fmax3(mx[0], s[124], s[125]);
+        mx[1] = fmax3(mx[1], s[126], s[127]);
+        const float rmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
         const float m_cand = fmaxf(m, rmax * sl2);
         const bool need = (m_cand - m) > p.rescale_thr;
         float alpha = 1.f;
@@ -426,32 +452,63 @@ __global__ void __launch_bounds__(320, 1)
           alpha = ex2_approx(m - m_cand);
           m = m_cand;
         }
-        const float neg_m = -m;
-        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+        // P = 2^(S*scale*log2e - m), rounded to the MMA's 16-bit type.  Two
+        // row sums: of the fp32 values (for the logsumexp) and, for bf16, of
+        // the rounded values the PV MMA actually multiplies V with, which is
+        // what O is normalised by (the weights then sum to one exactly).
+        const uint64_t sl2_2 = f2(sl2, sl2);
+        const uint64_t negm_2 = f2(-m, -m);
+        uint64_t sx2[2] = {0, 0}, sr2[2] = {0, 0};
         uint32_t pk[2][32];
 #pragma unroll
         for (int c = 0; c < 128; c += 2) {
-          const float p0 = ex2_approx(fmaf(s[c], sl2, neg_m));
-          const float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg_m));
-          sum[(c >> 1) & 3] += p0 + p1;
-          pk[c >> 6][(c >> 1) & 31] = pack2<BF16>(p0, p1);
+          float x0, x1;
+          f2_split(ffma2(f2(s[c], s[c + 1]), sl2_2, negm_2), x0, x1);
+          const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+          const uint32_t pp = pack2<BF16>(e0, e1);
+          pk[c >> 6][(c >> 1) & 31] = pp;
+          sx2[(c >> 1) & 1] = fadd2(sx2[(c >> 1) & 1], f2(e0, e1));
+          if constexpr (BF16) sr2[(c >> 1) & 1] = fadd2(sr2[(c >> 1) & 1], unpack2<BF16>(pp));
+        }
+        float sum_x, sum_r;
+        {
+          float a, b;
+          f2_split(fadd2(sx2[0], sx2[1]), a, b);
+          sum_x = a + b;
+          if constexpr (BF16) {
+            f2_split(fadd2(sr2[0], sr2[1]), a, b);
+            sum_r = a + b;
+          } else {
+            sum_r = sum_x;
+          }
         }
         tmem_st32(tS + 0, pk[0]);
         tmem_st32(tS + 32, pk[1]);
-        l = l * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+        l = l * alpha + sum_x;
+        lr = lr * alpha + sum_r;
         // Conditional rescale of the running output (v4 pseudo-code panel:
         // "if need_rescale(m, m_new): acc *= exp(m - m_new)"), done once the
         // S values are no longer live.  PV(j-1) is complete: its commit
         // precedes this block's S commit; PV(j) waits for this group's signal.
         if (j > 0 && __any_sync(0xffffffffu, need)) {
+          uint32_t orr[D / 32][32];
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + 32 * c, orr[c]);
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) tmem_ld_wait(orr[c]);
+          const uint64_t alpha2 = f2(alpha, alpha);
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
-            uint32_t orr[32];
-            tmem_ld32(tO + 32 * c, orr);
-            tmem_ld_wait(orr);
 #pragma unroll
-            for (int u = 0; u < 32; ++u) orr[u] = __float_as_uint(__uint_as_float(orr[u]) * alpha);
-            tmem_st32(tO + 32 * c, orr);
+            for (int u = 0; u < 32; u += 2) {
+              float a, b;
+              f2_split(fmul2(f2(__uint_as_float(orr[c][u]), __uint_as_float(orr[c][u + 1])),
+                             alpha2),
+                       a, b);
+              orr[c][u] = __float_as_uint(a);
+              orr[c][u + 1] = __float_as_uint(b);
+            }
+            tmem_st32(tO + 32 * c, orr[c]);
           }
         }
         tmem_st_wait();
@@ -466,7 +523,8 @@ __global__ void __launch_bounds__(320, 1)
       if (!ok) break;
       o_phase ^= 1u;
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / lr;
+      const uint64_t inv_l2 = f2(inv_l, inv_l);
       const bool live = q_idx < p.N;
       const size_t row_off = (static_cast<size_t>(it.bh) * p.N + q_idx);
       uint4 *orow = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + row_off * D);
@@ -477,9 +535,12 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld_wait(orr);
         uint32_t pk16[16];
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-          pk16[u] = pack2<BF16>(__uint_as_float(orr[2 * u]) * inv_l,
-                                __uint_as_float(orr[2 * u + 1]) * inv_l);
+        for (int u = 0; u < 16; ++u) {
+          float a, b;
+          f2_split(fmul2(f2(__uint_as_float(orr[2 * u]), __uint_as_float(orr[2 * u + 1])), inv_l2),
+                   a, b);
+          pk16[u] = pack2<BF16>(a, b);
+        }
         if (live) {
 #pragma unroll
           for (int u = 0; u < 4; ++u)

@@ -56,8 +56,14 @@ typedef void *fa_stream_t;
 #define FA_ERR_CUDA (-8)           /* a CUDA runtime/driver call failed */
 #define FA_ERR_TIMEOUT (-9)        /* a pipeline wait inside the kernel gave up */
 #define FA_ERR_ALIAS (-10)         /* an output overlaps an input or the other output */
+#define FA_ERR_OPTION (-11)        /* rescale_threshold outside [0, FA_MAX_RESCALE_THRESHOLD] */
 
 #define FA_MAX_N (1 << 20)         /* longest sequence accepted */
+
+/* Rescale threshold used by fa_fwd and fa_fwd_fp16, in log2 units of the
+ * scaled logits (see fa_fwd_ex). */
+#define FA_DEFAULT_RESCALE_THRESHOLD 8.0f
+#define FA_MAX_RESCALE_THRESHOLD 12.0f
 
 /*
  * fa_fwd -- attention forward on bf16 inputs.
@@ -75,10 +81,34 @@ typedef void *fa_stream_t;
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
            int64_t H, int64_t N, int64_t d, int causal, float scale, fa_stream_t stream);
 
-/* fa_fwd_fp16 -- identical to fa_fwd with fp16 q, k, v and o. */
+/* fa_fwd_fp16 -- identical to fa_fwd with fp16 q, k, v and o.
+ * Both use the rescale threshold FA_DEFAULT_RESCALE_THRESHOLD (fa_fwd_ex). */
 int fa_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
                 int64_t H, int64_t N, int64_t d, int causal, float scale,
                 fa_stream_t stream);
+
+/*
+ * fa_fwd_ex -- fa_fwd / fa_fwd_fp16 with the online-softmax rescale rule
+ * exposed (FlashAttention v4 Blackwell pipeline diagram, pseudo-code panel:
+ * "maybe skip rescale if max change small"; softmax and correction lanes:
+ * rescale the old accumulator only when the max change calls for it).
+ *
+ *   fp16              : 0 = bf16 q/k/v/o, 1 = fp16
+ *   rescale_threshold : tau >= 0 in log2 units of the scaled logits.  For
+ *       each query row, the running max m used to form P = 2^(S*log2e*scale
+ *       - m) is raised (and O, l rescaled by 2^(m_old - m_new)) only when a
+ *       block's max exceeds m by more than tau; otherwise m is kept and the
+ *       block's probabilities may reach 2^tau.  Numerator and denominator
+ *       use the same m, so the result is the same softmax for any tau; tau
+ *       = 0 rescales whenever the max grows ("skip when the max does not
+ *       change").  Must lie in [0, FA_MAX_RESCALE_THRESHOLD] so 2^tau stays
+ *       far inside the fp16 range of P; otherwise FA_ERR_OPTION.
+ *
+ * All other arguments, the layout and the error behaviour are fa_fwd's.
+ */
+int fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+              int64_t H, int64_t N, int64_t d, int causal, float scale, int fp16,
+              float rescale_threshold, fa_stream_t stream);
 
 /*
  * fa_get_status -- synchronises `stream`, then returns and clears the

@@ -27,7 +27,8 @@ def declared_functions():
 
 def test_header_declares_entry_points():
     names = declared_functions()
-    for n in ("fa_fwd", "fa_fwd_fp16", "fa_get_status", "fa_strerror", "fa_version"):
+    for n in ("fa_fwd", "fa_fwd_fp16", "fa_fwd_ex", "fa_get_status", "fa_strerror",
+              "fa_version"):
         assert n in names
 
 
@@ -38,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_version_and_strerror(lib):
     assert lib.fa_version() == 100
-    for code in range(0, -11, -1):
+    for code in range(0, -12, -1):
         msg = fa.fa_strerror(code)
         assert msg and msg != "unknown error code"
     assert fa.fa_strerror(-999) == "unknown error code"
@@ -85,3 +86,18 @@ def test_python_binding_rejects_cpu_tensors(lib):
     q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.fa_fwd(q, q, q, q.clone(), torch.zeros(1, 1, 128))
+
+
+def test_fa_fwd_ex_option_errors(lib):
+    def ex(thr, **kw):
+        a = dict(q=Q, k=K, v=V, o=O, lse=L, B=1, H=1, N=128, d=64, causal=0, scale=0.125,
+                 fp16=0)
+        a.update(kw)
+        return lib.fa_fwd_ex(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
+                             a["d"], a["causal"], a["scale"], a["fp16"], thr, None)
+    assert ex(-0.5) == fa.FA_ERR_OPTION
+    assert ex(12.5) == fa.FA_ERR_OPTION
+    assert ex(float("nan")) == fa.FA_ERR_OPTION
+    assert ex(float("inf")) == fa.FA_ERR_OPTION
+    assert ex(8.0, q=None) == fa.FA_ERR_NULL
+    assert ex(8.0, d=32, fp16=1) == fa.FA_ERR_HEADDIM

@@ -31,10 +31,10 @@ def fa():
     return m
 
 
-def run_gpu(q, k, v, causal, scale=None, stream=None):
+def run_gpu(q, k, v, causal, scale=None, stream=None, rescale_threshold=None):
     dev = torch.device("cuda")
     o, lse = fa().forward(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=scale,
-                          stream=stream)
+                          stream=stream, rescale_threshold=rescale_threshold)
     torch.cuda.synchronize()
     assert fa().fa_get_status() == 0
     return o.float().cpu().numpy(), lse.cpu().numpy()
@@ -175,3 +175,32 @@ def test_caller_buffers_and_no_write_on_error():
     fa().fa_fwd(q, k, v, o, lse, causal=False)
     torch.cuda.synchronize()
     assert not torch.any(o == 7.0)
+
+
+@pytest.mark.parametrize("thr", [0.0, 3.0, 8.0, 12.0])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("dtype,k_mult", [(torch.bfloat16, 1.0), (torch.float16, 4.0),
+                                          (torch.bfloat16, 6.0)], ids=["bf16", "fp16x4", "bf16x6"])
+def test_rescale_threshold_parity(thr, causal, dtype, k_mult):
+    """Every rescale threshold gives the same softmax (numerator and
+    denominator share the stale max), including 0 = rescale whenever the
+    running max grows and peaked rows (K scaled up) that force rescales."""
+    q, k, v = make_qkv(2, 3, 1100, 128, dtype, seed=31, k_mult=k_mult)
+    o, lse = run_gpu(q, k, v, causal, rescale_threshold=thr)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 1.0 / math.sqrt(128))
+    assert_close(o, lse, o_ref, lse_ref, f"thr={thr}")
+
+
+def test_sorted_keys_force_rescale_every_block():
+    """Keys whose logits grow block after block make the running max rise on
+    every block, so the O rescale runs on every block for every row."""
+    B, H, N, d = 1, 2, 1024, 64
+    q = torch.ones(B, H, N, d)
+    k = torch.linspace(0, 3.0, N).view(1, 1, N, 1).expand(B, H, N, d).contiguous()
+    _, _, v = make_qkv(B, H, N, d, torch.float32, seed=32)
+    q, k, v = (x.to(torch.bfloat16) for x in (q, k, v))
+    for thr in (0.0, 8.0):
+        for causal in (False, True):
+            o, lse = run_gpu(q, k, v, causal, rescale_threshold=thr)
+            o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 1.0 / math.sqrt(d))
+            assert_close(o, lse, o_ref, lse_ref, f"sorted keys thr={thr} causal={causal}")
