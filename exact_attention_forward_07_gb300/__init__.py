@@ -71,6 +71,8 @@ def lib():
         L.fa_fwd_ex.argtypes = [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int, ctypes.c_float,
                                 ctypes.c_int, ctypes.c_float, P]
         L.fa_fwd_ex.restype = ctypes.c_int
+        L.fa_selftest_wait_timeout.argtypes = [I64, P, P]
+        L.fa_selftest_wait_timeout.restype = ctypes.c_int
         L.fa_get_status.argtypes = [P]
         L.fa_get_status.restype = ctypes.c_int
         L.fa_strerror.argtypes = [ctypes.c_int]

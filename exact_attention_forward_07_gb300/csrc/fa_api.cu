@@ -216,6 +216,19 @@ int fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, 
                     stream);
 }
 
+int fa_selftest_wait_timeout(int64_t timeout_us, int *gave_up, fa_stream_t stream) {
+  if (!gave_up) return FA_ERR_NULL;
+  if (timeout_us < 1 || timeout_us > 1000000) return FA_ERR_OPTION;
+  DeviceState *ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != FA_OK) return rc;
+  fa::fa_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      ds->status, static_cast<uint64_t>(timeout_us) * 1000u, gave_up);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
 int fa_get_status(fa_stream_t stream) {
   DeviceState *ds = nullptr;
   int rc = device_state(&ds);
@@ -247,7 +260,9 @@ const char *fa_strerror(int code) {
     case FA_ERR_CUDA: return "a CUDA runtime or driver call failed (see fa_last_cuda_error)";
     case FA_ERR_TIMEOUT: return "a pipeline wait inside the kernel gave up; outputs undefined";
     case FA_ERR_ALIAS: return "an output buffer overlaps an input or the other output";
-    case FA_ERR_OPTION: return "rescale_threshold must lie in [0, FA_MAX_RESCALE_THRESHOLD]";
+    case FA_ERR_OPTION:
+      return "option out of range (rescale_threshold in [0, FA_MAX_RESCALE_THRESHOLD], "
+             "self-test limit in [1, 1e6] us)";
     default: return "unknown error code";
   }
 }

@@ -127,13 +127,13 @@ __device__ __forceinline__ int round_item(int round, const Params &p) {
 }
 
 __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                       unsigned *status) {
+                                          unsigned *status, uint64_t timeout_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kTimeoutNs) {
+      if (globaltimer_ns() - t0 > timeout_ns) {
         *abort_flag = 1;
         atomicOr(status, kStatusTimeout);
         return false;
@@ -144,9 +144,9 @@ __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatil
 
 // Bounded wait for phase `parity` of barrier `bar`; false = give up.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                         unsigned *status) {
+                                         unsigned *status, uint64_t timeout_ns = kTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
-  return wait_slow(bar, parity, abort_flag, status);
+  return wait_slow(bar, parity, abort_flag, status, timeout_ns);
 }
 
 // Drain wait: bounded by time only (the awaited copy or MMA needs nothing
@@ -558,6 +558,22 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+}
+
+// Self-test of the failure path: one warp waits on a barrier that nothing
+// ever arrives on.  The bounded wait must give up after `timeout_ns`, set
+// the status word and return, leaving the context usable.
+__global__ void fa_wait_selftest_kernel(unsigned *status, uint64_t timeout_ns, int *gave_up) {
+  __shared__ __align__(8) uint64_t never;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&never), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const bool ok = wait_bar(smem_u32(&never), 0, &abort_flag, status, timeout_ns);
+  if (threadIdx.x == 0) *gave_up = ok ? 0 : 1;
 }
 
 }  // namespace fa

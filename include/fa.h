@@ -56,7 +56,7 @@ typedef void *fa_stream_t;
 #define FA_ERR_CUDA (-8)           /* a CUDA runtime/driver call failed */
 #define FA_ERR_TIMEOUT (-9)        /* a pipeline wait inside the kernel gave up */
 #define FA_ERR_ALIAS (-10)         /* an output overlaps an input or the other output */
-#define FA_ERR_OPTION (-11)        /* rescale_threshold outside [0, FA_MAX_RESCALE_THRESHOLD] */
+#define FA_ERR_OPTION (-11)        /* an option (rescale threshold, self-test limit) out of range */
 
 #define FA_MAX_N (1 << 20)         /* longest sequence accepted */
 
@@ -117,6 +117,17 @@ int fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, 
  * undefined).  FA_ERR_CUDA if the synchronisation itself failed.
  */
 int fa_get_status(fa_stream_t stream);
+
+/*
+ * fa_selftest_wait_timeout -- exercises the kernels' failure path without a
+ * fault: launches one warp that waits, with the same bounded wait the
+ * attention kernel uses, on a barrier nothing ever arrives on.  After
+ * timeout_us microseconds (1 .. 1e6) the wait gives up, writes 1 to the
+ * device int *gave_up, sets the status word (so the next fa_get_status
+ * returns FA_ERR_TIMEOUT) and the kernel returns normally.  Asynchronous on
+ * `stream`.  FA_ERR_NULL / FA_ERR_OPTION on bad arguments.
+ */
+int fa_selftest_wait_timeout(int64_t timeout_us, int *gave_up, fa_stream_t stream);
 
 /* fa_strerror -- static, human-readable text for a FA_* code. */
 const char *fa_strerror(int code);

@@ -101,3 +101,9 @@ def test_fa_fwd_ex_option_errors(lib):
     assert ex(float("inf")) == fa.FA_ERR_OPTION
     assert ex(8.0, q=None) == fa.FA_ERR_NULL
     assert ex(8.0, d=32, fp16=1) == fa.FA_ERR_HEADDIM
+
+
+def test_selftest_argument_errors(lib):
+    assert lib.fa_selftest_wait_timeout(1000, None, None) == fa.FA_ERR_NULL
+    assert lib.fa_selftest_wait_timeout(0, 0x10000000, None) == fa.FA_ERR_OPTION
+    assert lib.fa_selftest_wait_timeout(2000000, 0x10000000, None) == fa.FA_ERR_OPTION

@@ -204,3 +204,21 @@ def test_sorted_keys_force_rescale_every_block():
             o, lse = run_gpu(q, k, v, causal, rescale_threshold=thr)
             o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 1.0 / math.sqrt(d))
             assert_close(o, lse, o_ref, lse_ref, f"sorted keys thr={thr} causal={causal}")
+
+
+def test_bounded_wait_gives_up_and_context_survives():
+    """Failure detection without a fault: a wait that nothing satisfies gives
+    up after its limit, the status word reports FA_ERR_TIMEOUT once (then is
+    cleared), and the context still runs a correct forward afterwards."""
+    gave_up = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert fa().fa_get_status() == 0
+    rc = fa().lib().fa_selftest_wait_timeout(20000, gave_up.data_ptr(), None)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert gave_up.item() == 1
+    assert fa().fa_get_status() == fa().FA_ERR_TIMEOUT
+    assert fa().fa_get_status() == 0
+    q, k, v = make_qkv(1, 2, 256, 64, torch.bfloat16, seed=12)
+    o, lse = run_gpu(q, k, v, True)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, True, 1.0 / 8.0)
+    assert_close(o, lse, o_ref, lse_ref, "after timeout self-test")
