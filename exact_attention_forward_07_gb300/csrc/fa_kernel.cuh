@@ -26,7 +26,7 @@
 //
 // MMA issue order per K/V block j (ping-pong between the two Q tiles, so one
 // group's softmax overlaps the other group's MMAs):
-//   PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
+//   S0_{j+1}, PV1_j, S1_{j+1}, PV0_{j+1}
 // Each S_t commit also covers the PV_t issued before it, so a softmax group
 // that sees S_t(j+1) ready may rescale O_t (PV_t(j) is complete) and the
 // MMA does not issue PV_t(j+1) until that group signals P_t ready.
@@ -292,25 +292,31 @@ __global__ void __launch_bounds__(384, 1)
           phase ^= 1u;
         }
       };
+      // Descriptors are built once; per MMA only the K-step offset (in
+      // 16-byte units, inside the 14-bit address field) is added.
+      const uint64_t kdesc0 = smem_desc_sw128(0, 16, 1024);             // Q, K: K-major
+      const uint64_t vdesc0 = smem_desc_sw128(0, C::kHalfBytes, 1024);  // V: MN-major
       auto issue_s = [&](int t, uint32_t kslot) {
-        const uint32_t q_addr = sbase + C::kQOff + t * C::kTileBytes;
-        const uint32_t k_addr = sbase + C::kKVOff + kslot * C::kTileBytes;
+        const uint64_t qd = kdesc0 + ((sbase + C::kQOff + t * C::kTileBytes) >> 4);
+        const uint64_t kd = kdesc0 + ((sbase + C::kKVOff + kslot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::col_s(t), smem_desc_sw128(q_addr + off, 16, 1024),
-                 smem_desc_sw128(k_addr + off, 16, 1024), C::kIdescS, kk > 0);
+          const uint32_t off = ((kk >> 2) * C::kHalfBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::col_s(t), qd + off, kd + off, C::kIdescS, kk > 0);
         }
       };
       auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
-        const uint32_t v_addr = sbase + C::kKVOff + vslot * C::kTileBytes;
+        const uint64_t vd = vdesc0 + ((sbase + C::kKVOff + vslot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk) {
-          mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8,
-                 smem_desc_sw128(v_addr + kk * 2048, C::kHalfBytes, 1024), C::kIdescO,
-                 (acc || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, vd + kk * (2048 >> 4),
+                 C::kIdescO, (acc || kk > 0) ? 1u : 0u);
         }
       };
+      // The loop is rotated so that the iteration boundary (and the release
+      // of a K slot) falls right after PV0's MMAs are queued: between the end
+      // of S1's issue and the start of PV0's there is then only one commit
+      // and one wait, and the tensor core's short queue does not run dry.
       for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_items; ++round) {
         const int item = round_item(round, p);
         if (item < 0) continue;
@@ -333,39 +339,45 @@ __global__ void __launch_bounds__(384, 1)
         }
         mma_commit(bar(C::kKVEmpty + ks));
         if (n_max == 1) mma_commit(bar(C::kQEmpty));
+        // PV0(0) (tile 0 always has at least one block)
+        if (!(ok = wait_bar(bar(C::kKVFull + vs), vph, abort_flag, p.status))) break;
+        if (!(ok = wait_bar(bar(C::kPFull + 0), p_phase[0], abort_flag, p.status))) break;
+        p_phase[0] ^= 1u;
+        tc_fence_after();
+        issue_pv(0, vs, false);
         for (int j = 0; j < n_max; ++j) {
-          if (!(ok = wait_bar(bar(C::kKVFull + vs), vph, abort_flag, p.status))) break;
+          // queued: PV0(j)
           const bool more = j + 1 < n_max;
           if (more) {
             ks = slot;
             kph = phase;
             advance();
-          }
-          // tile 0
-          if (j < it.n0) {
-            if (!(ok = wait_bar(bar(C::kPFull + 0), p_phase[0], abort_flag, p.status))) break;
-            p_phase[0] ^= 1u;
-            tc_fence_after();
-            issue_pv(0, vs, j > 0);
-          }
-          if (more) {
             if (!(ok = wait_bar(bar(C::kKVFull + ks), kph, abort_flag, p.status))) break;
             tc_fence_after();
           }
+          // tile 0: S0(j+1), or the end of tile 0 (PV0(n0-1) is already queued)
           if (j + 1 < it.n0) {
             issue_s(0, ks);
             mma_commit(bar(C::kSFull + 0));
           } else if (j + 1 == it.n0) {
             mma_commit(bar(C::kOFull + 0));
           }
-          // tile 1
+          // tile 1: PV1(j)
           if (j < it.n1) {
             if (!(ok = wait_bar(bar(C::kPFull + 1), p_phase[1], abort_flag, p.status))) break;
             p_phase[1] ^= 1u;
             tc_fence_after();
             issue_pv(1, vs, j > 0);
           }
-          mma_commit(bar(C::kKVEmpty + vs));
+          mma_commit(bar(C::kKVEmpty + vs));  // V_j read by PV0(j) and PV1(j)
+          uint32_t nvs = 0;
+          if (more) {  // V_{j+1}: checked now, before S1's MMAs fill the queue
+            nvs = slot;
+            const uint32_t nvph = phase;
+            advance();
+            if (!(ok = wait_bar(bar(C::kKVFull + nvs), nvph, abort_flag, p.status))) break;
+          }
+          // tile 1: S1(j+1), or the end of tile 1
           if (j + 1 < it.n1) {
             issue_s(1, ks);
             mma_commit(bar(C::kSFull + 1));
@@ -373,11 +385,16 @@ __global__ void __launch_bounds__(384, 1)
             mma_commit(bar(C::kOFull + 1));
           }
           if (more) {
-            mma_commit(bar(C::kKVEmpty + ks));
+            // tile 0: PV0(j+1)
+            if (j + 1 < it.n0) {
+              if (!(ok = wait_bar(bar(C::kPFull + 0), p_phase[0], abort_flag, p.status))) break;
+              p_phase[0] ^= 1u;
+              tc_fence_after();
+              issue_pv(0, nvs, true);
+            }
+            mma_commit(bar(C::kKVEmpty + ks));  // K_{j+1} read by S0(j+1) and S1(j+1)
             if (j + 2 == n_max) mma_commit(bar(C::kQEmpty));
-            vs = slot;
-            vph = phase;
-            advance();
+            vs = nvs;
           }
         }
       }
@@ -452,34 +469,32 @@ __global__ void __launch_bounds__(384, 1)
           alpha = ex2_approx(m - m_cand);
           m = m_cand;
         }
-        // P = 2^(S*scale*log2e - m), rounded to the MMA's 16-bit type.  Two
-        // row sums: of the fp32 values (for the logsumexp) and, for bf16, of
-        // the rounded values the PV MMA actually multiplies V with, which is
-        // what O is normalised by (the weights then sum to one exactly).
+        // P = 2^(S*scale*log2e - m), rounded to the MMA's 16-bit type.  The
+        // logsumexp uses the fp32 row sum.  O is normalised by that sum plus,
+        // for bf16, the rounding error of the block's largest P: in a peaked
+        // row the dominant weight's rounding would otherwise show in O
+        // undivided, while the other elements' rounding errors average out.
         const uint64_t sl2_2 = f2(sl2, sl2);
         const uint64_t negm_2 = f2(-m, -m);
-        uint64_t sx2[2] = {0, 0}, sr2[2] = {0, 0};
+        uint64_t sx2[2] = {0, 0};
         uint32_t pk[2][32];
 #pragma unroll
         for (int c = 0; c < 128; c += 2) {
           float x0, x1;
           f2_split(ffma2(f2(s[c], s[c + 1]), sl2_2, negm_2), x0, x1);
           const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-          const uint32_t pp = pack2<BF16>(e0, e1);
-          pk[c >> 6][(c >> 1) & 31] = pp;
+          pk[c >> 6][(c >> 1) & 31] = pack2<BF16>(e0, e1);
           sx2[(c >> 1) & 1] = fadd2(sx2[(c >> 1) & 1], f2(e0, e1));
-          if constexpr (BF16) sr2[(c >> 1) & 1] = fadd2(sr2[(c >> 1) & 1], unpack2<BF16>(pp));
         }
         float sum_x, sum_r;
         {
           float a, b;
           f2_split(fadd2(sx2[0], sx2[1]), a, b);
           sum_x = a + b;
+          sum_r = sum_x;
           if constexpr (BF16) {
-            f2_split(fadd2(sr2[0], sr2[1]), a, b);
-            sum_r = a + b;
-          } else {
-            sum_r = sum_x;
+            const float top = ex2_approx(fmaf(rmax, sl2, -m));  // the block's largest P
+            sum_r += __bfloat162float(__float2bfloat16_rn(top)) - top;
           }
         }
         tmem_st32(tS + 0, pk[0]);
