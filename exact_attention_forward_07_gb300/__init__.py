@@ -16,8 +16,8 @@ import ctypes
 import math
 import os
 
-__all__ = ["FaError", "fa_fwd", "fa_fwd_fp16", "fa_fwd_ex", "fa_get_status", "fa_strerror", "fa_version",
-           "forward", "library_path", "lib"]
+__all__ = ["FaError", "HostPipeline", "fa_fwd", "fa_fwd_fp16", "fa_fwd_ex", "fa_get_status",
+           "fa_strerror", "fa_version", "forward", "library_path", "lib"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
@@ -177,3 +177,71 @@ def forward(q, k, v, causal=False, scale=None, stream=None, rescale_threshold=No
     else:
         raise TypeError(f"unsupported dtype {q.dtype}: use bfloat16 or float16")
     return o, lse
+
+
+class HostPipeline:
+    """Forward on pinned host buffers, pipelined over chunks of heads.
+
+    Every (batch, head) is independent, so the [B*H, N, d] tensors are cut
+    into chunks of heads; chunk c's host->device copy, chunk c-1's forward
+    and chunk c-2's device->host copy run on different streams (and copy
+    engines) at the same time.  Device staging buffers for `depth` chunks
+    are allocated once, here; each call copies, computes (fa_fwd /
+    fa_fwd_fp16 through the C ABI) and copies back, then synchronises.
+    """
+
+    def __init__(self, B, H, N, d, dtype, device=None, chunks=4, depth=3):
+        import torch
+        self.B, self.H, self.N, self.d = B, H, N, d
+        self.dtype = dtype
+        self.device = torch.device(device or "cuda")
+        bh = B * H
+        self.nchunks = max(1, min(int(chunks), bh))
+        self.bounds = [bh * c // self.nchunks for c in range(self.nchunks + 1)]
+        width = max(self.bounds[c + 1] - self.bounds[c] for c in range(self.nchunks))
+        self.depth = max(1, min(int(depth), self.nchunks))
+        self.bufs = []
+        for _ in range(self.depth):
+            mk = lambda: torch.empty((width, 1, N, d), dtype=dtype, device=self.device)
+            self.bufs.append(dict(q=mk(), k=mk(), v=mk(), o=mk(),
+                                  lse=torch.empty((width, 1, N), dtype=torch.float32,
+                                                  device=self.device)))
+        self.h2d = [torch.cuda.Stream(self.device) for _ in range(self.depth)]
+        self.comp = [torch.cuda.Stream(self.device) for _ in range(self.depth)]
+        self.d2h = [torch.cuda.Stream(self.device) for _ in range(self.depth)]
+        self.free = [None] * self.depth
+
+    def __call__(self, q, k, v, o, lse, causal=False, scale=None):
+        """q, k, v, o: pinned CPU [B,H,N,d]; lse: pinned CPU [B,H,N] fp32."""
+        import torch
+        bh, N, d = self.B * self.H, self.N, self.d
+        qf, kf, vf, of = (x.view(bh, 1, N, d) for x in (q, k, v, o))
+        lf = lse.view(bh, 1, N)
+        fn = fa_fwd if self.dtype == torch.bfloat16 else fa_fwd_fp16
+        for c in range(self.nchunks):
+            a, b = self.bounds[c], self.bounds[c + 1]
+            n = b - a
+            i = c % self.depth
+            buf = self.bufs[i]
+            s_in, s_cp, s_out = self.h2d[i], self.comp[i], self.d2h[i]
+            if self.free[i] is not None:
+                s_in.wait_event(self.free[i])
+            with torch.cuda.stream(s_in):
+                for name, src in (("q", qf), ("k", kf), ("v", vf)):
+                    buf[name][:n].copy_(src[a:b], non_blocking=True)
+                loaded = torch.cuda.Event()
+                loaded.record(s_in)
+            s_cp.wait_event(loaded)
+            with torch.cuda.stream(s_cp):
+                fn(buf["q"][:n], buf["k"][:n], buf["v"][:n], buf["o"][:n], buf["lse"][:n],
+                   causal=causal, scale=scale, stream=s_cp)
+                done = torch.cuda.Event()
+                done.record(s_cp)
+            s_out.wait_event(done)
+            with torch.cuda.stream(s_out):
+                of[a:b].copy_(buf["o"][:n], non_blocking=True)
+                lf[a:b].copy_(buf["lse"][:n], non_blocking=True)
+                self.free[i] = torch.cuda.Event()
+                self.free[i].record(s_out)
+        for s in self.d2h:
+            s.synchronize()

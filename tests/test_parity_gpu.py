@@ -222,3 +222,20 @@ def test_bounded_wait_gives_up_and_context_survives():
     o, lse = run_gpu(q, k, v, True)
     o_ref, lse_ref = oracle.attn_fwd(q, k, v, True, 1.0 / 8.0)
     assert_close(o, lse, o_ref, lse_ref, "after timeout self-test")
+
+
+@pytest.mark.parametrize("chunks,depth", [(1, 1), (3, 2), (5, 3)])
+def test_host_pipeline_matches_oracle(chunks, depth):
+    """The pipelined host-buffer forward (chunks of heads on several streams)
+    gives the oracle's result, twice in a row with reused staging buffers."""
+    B, H, N, d = 2, 5, 333, 128
+    q, k, v = make_qkv(B, H, N, d, torch.bfloat16, seed=40)
+    pin = [x.pin_memory() for x in (q, k, v)]
+    pipe = fa().HostPipeline(B, H, N, d, torch.bfloat16, "cuda", chunks=chunks, depth=depth)
+    for causal in (True, False):
+        o = torch.empty_like(q).pin_memory()
+        lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+        pipe(*pin, o, lse, causal=causal)
+        assert fa().fa_get_status() == 0
+        o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 1.0 / math.sqrt(d))
+        assert_close(o.float().numpy(), lse.numpy(), o_ref, lse_ref, f"pipeline {chunks}/{depth}")
