@@ -10,9 +10,12 @@
 //
 // Roles inside the CTA (FlashAttention v4 Blackwell pipeline diagram, the
 // producer / MMA / softmax lanes and the pseudo-code panel):
-//   warps 0-3  softmax group 0: online softmax of Q tile 0, its O rescale and
-//              its epilogue (O / l, logsumexp)
-//   warps 4-7  softmax group 1: the same for Q tile 1
+//   warps 0-7  softmax: online softmax, O rescale and epilogue (O / l,
+//              logsumexp).  Two organisations (template SPLIT):
+//              false: warps 0-3 own Q tile 0, warps 4-7 own Q tile 1;
+//              true:  all eight warps take both tiles' S in turn, warps w and
+//              w + 4 splitting the columns of the rows of lane quadrant w % 4
+//              (about half the softmax latency per tile; used for d = 128)
 //   warp  8    MMA issue (one thread) + tensor-memory allocation
 //   warp  9    TMA producer (one thread): Q tiles and a K/V ring
 //   warps 10-11 idle (they complete the third warpgroup, whose registers
@@ -77,7 +80,8 @@ struct Cfg {
   static constexpr int kDrain = kOFull + 2;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
-  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
+  static constexpr int kXchOff = (kMiscOff + 16 + 15) & ~15;  // softmax row exchange, 4 KB
+  static constexpr int kSmemBytes = kXchOff + 2 * 2 * 2 * 128 * 4 + 1024;  // + base alignment slack
   static constexpr uint32_t kTmemCols = 512;
   // tensor-memory column of S_t and O_t for Q tile t
   static __device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
@@ -180,7 +184,7 @@ __device__ __forceinline__ uint64_t unpack2(uint32_t v) {
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool SPLIT>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -208,7 +212,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(bar(C::kQEmpty), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::kSFull + t), 1);
-      mbar_init(bar(C::kPFull + t), 4);  // one arrive per softmax warp
+      mbar_init(bar(C::kPFull + t), SPLIT ? 8 : 4);  // one arrive per softmax warp
       mbar_init(bar(C::kOFull + t), 1);
     }
     mbar_init(bar(C::kDrain), 1);
@@ -405,7 +409,10 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else {
     regs_inc<C::kRegsSoftmax>();
-    // ---------------------------------------------------- softmax groups
+    if constexpr (!SPLIT) {
+    // ------------------------------------------ softmax, one group per tile
+    // Warps 0-3 handle Q tile 0 and warps 4-7 Q tile 1, one thread per row,
+    // all 128 columns; the two groups run their tiles concurrently.
     const int t = warp >> 2;                      // Q tile of this group
     const uint32_t lane_base = (warp & 3) * 32u;  // this warp's TMEM lane quadrant
     const int row = static_cast<int>(lane_base + lane);
@@ -566,6 +573,224 @@ __global__ void __launch_bounds__(384, 1)
       if (live) p.lse[row_off] = (m + lg2_approx(l)) * 0.6931471805599453f;
     }
     tc_fence_before();
+    } else {
+    // ------------------------------------------ softmax, column split
+    // All eight softmax warps work on whichever tile's S is ready (S0(j),
+    // S1(j), S0(j+1), ... in the order the MMAs produce them).  Warp w takes
+    // the 32 rows of tensor-memory lane quadrant q = w % 4 (one thread per
+    // row) and the 64 columns [64h, 64h + 64) of S, h = w / 4, so two warps
+    // share each SMSP's rows and the softmax of one tile takes about half
+    // as long.  The two warps of a quadrant exchange partial row maxima
+    // (and, at the end, partial row sums) through shared memory.
+    const int q = warp & 3, hf = warp >> 2;
+    const uint32_t lane_base = q * 32u;
+    const int row = static_cast<int>(lane_base + lane);
+    const uint32_t t_lane = tmem + (lane_base << 16);
+    float *xch = reinterpret_cast<float *>(smem + C::kXchOff);  // [parity][half][value][row]
+    auto xslot = [&](uint32_t par, int h, int val) { return xch + ((par * 2 + h) * 2 + val) * 128 + row; };
+    const uint32_t pair_bar = 1u + static_cast<uint32_t>(q);  // named barrier of the quadrant's two warps
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
+    const float sl2 = p.scale_log2;
+    uint32_t s_par = 0, o_par = 0, xpar = 0;  // barrier phase bits per tile, exchange parity
+    // bar.sync cannot time out, so a warp whose wait gave up (ok == false)
+    // keeps walking the same sequence of blocks, doing no work but taking
+    // part in every pair barrier, so its partner can never be left waiting.
+    bool ok = true;
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.n_items; ++round) {
+      const int item = round_item(round, p);
+      if (item < 0) continue;
+      const Item it = decode_item(item, p);
+      const int n_max = it.n0 > it.n1 ? it.n0 : it.n1;
+      // per tile: running max (log2 units), this half's sums of P and of P
+      // corrected for the rounding of each block's largest value
+      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, r0 = 0.f, r1 = 0.f;
+      // epilogue of tile t: O / l to memory, logsumexp (one pair barrier on
+      // every path, like a block)
+      auto epilogue = [&](int t) {
+        if (ok) ok = wait_bar(bar(C::kOFull + t), (o_par >> t) & 1u, abort_flag, p.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          pair_sync();
+          return;
+        }
+        o_par ^= 1u << t;
+        tc_fence_after();
+        *xslot(xpar, hf, 0) = t ? l1 : l0;
+        *xslot(xpar, hf, 1) = t ? r1 : r0;
+        pair_sync();
+        const float lsum = (t ? l1 : l0) + *xslot(xpar, hf ^ 1, 0);
+        const float rsum = (t ? r1 : r0) + *xslot(xpar, hf ^ 1, 1);
+        xpar ^= 1u;
+        const float inv_l = 1.f / rsum;
+        const uint64_t inv_l2 = f2(inv_l, inv_l);
+        const int q_idx = (it.qt0 + t) * 128 + row;
+        const bool live = q_idx < p.N;
+        const size_t row_off = (static_cast<size_t>(it.bh) * p.N + q_idx);
+        uint4 *orow = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + row_off * D +
+                                                (D / 2) * hf);
+        const uint32_t tO = t_lane + C::col_o(t) + (D / 2) * hf;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t orr[32];
+          tmem_ld32(tO + 32 * c, orr);
+          tmem_ld_wait(orr);
+          uint32_t pk16[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            float a, b;
+            f2_split(fmul2(f2(__uint_as_float(orr[2 * u]), __uint_as_float(orr[2 * u + 1])),
+                           inv_l2),
+                     a, b);
+            pk16[u] = pack2<BF16>(a, b);
+          }
+          if (live) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              orow[c * 4 + u] = make_uint4(pk16[4 * u], pk16[4 * u + 1], pk16[4 * u + 2],
+                                           pk16[4 * u + 3]);
+          }
+        }
+        if (live && hf == 0)
+          p.lse[row_off] = ((t ? m1 : m0) + lg2_approx(lsum)) * 0.6931471805599453f;
+      };
+      for (int j = 0; j < n_max; ++j) {
+        for (int t = 0; t < 2; ++t) {
+          if (j >= (t ? it.n1 : it.n0)) continue;
+          const int qt = it.qt0 + t;
+          if (ok) ok = wait_bar(bar(C::kSFull + t), (s_par >> t) & 1u, abort_flag, p.status);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) {  // failed: keep the pair barrier count in step, do nothing else
+            pair_sync();
+            continue;
+          }
+          s_par ^= 1u << t;
+          tc_fence_after();
+          const uint32_t tS = t_lane + C::col_s(t);
+          uint32_t sr[2][32];
+          tmem_ld32(tS + 64 * hf, sr[0]);
+          tmem_ld32(tS + 64 * hf + 32, sr[1]);
+          tmem_ld_wait(sr[0]);
+          tmem_ld_wait(sr[1]);
+          float s[64];
+#pragma unroll
+          for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+          // mask only where needed: the diagonal block (causal) or the ragged
+          // last block (non-causal, N % 128 != 0); c + 64h is the key column
+          if (p.causal && j == qt) {
+            const int lim = row - 64 * hf;
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c > lim) s[c] = -INFINITY;
+          } else if (!p.causal && j == p.n_qtiles - 1 && (p.N & 127)) {
+            const int lim = p.N - j * 128 - 64 * hf;
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c >= lim) s[c] = -INFINITY;
+          }
+          float mx[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+          for (int c = 4; c < 60; c += 8) {
+            mx[0] = fmax3(mx[0], s[c], s[c + 1]);
+            mx[1] = fmax3(mx[1], s[c + 2], s[c + 3]);
+            mx[2] = fmax3(mx[2], s[c + 4], s[c + 5]);
+            mx[3] = fmax3(mx[3], s[c + 6], s[c + 7]);
+          }
+          mx[0] = fmax3(mx[0], s[60], s[61]);
+          mx[1] = fmax3(mx[1], s[62], s[63]);
+          const float hmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);  // this half's max
+          *xslot(xpar, hf, 0) = hmax;
+          pair_sync();
+          const float rmax = fmaxf(hmax, *xslot(xpar, hf ^ 1, 0));
+          xpar ^= 1u;
+          float m = t ? m1 : m0;
+          const float m_cand = fmaxf(m, rmax * sl2);
+          const bool need = (m_cand - m) > p.rescale_thr;
+          float alpha = 1.f;
+          if (need) {
+            alpha = ex2_approx(m - m_cand);
+            m = m_cand;
+          }
+          // P = 2^(S*scale*log2e - m), rounded to the MMA's 16-bit type, over
+          // the P columns [32h, 32h + 32) of this tile (keys 64h..64h+63).
+          // Both warps have loaded their S halves (the exchange above), so the
+          // P stores cannot overwrite S the other warp still needs.
+          const uint64_t sl2_2 = f2(sl2, sl2);
+          const uint64_t negm_2 = f2(-m, -m);
+          uint64_t sx2[2] = {0, 0};
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            float x0, x1;
+            f2_split(ffma2(f2(s[c], s[c + 1]), sl2_2, negm_2), x0, x1);
+            const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+            pk[c >> 1] = pack2<BF16>(e0, e1);
+            sx2[(c >> 1) & 1] = fadd2(sx2[(c >> 1) & 1], f2(e0, e1));
+          }
+          tmem_st32(tS + 32 * hf, pk);
+          float sum_x, sum_r;
+          {
+            float a, b;
+            f2_split(fadd2(sx2[0], sx2[1]), a, b);
+            sum_x = a + b;
+            sum_r = sum_x;
+            if constexpr (BF16) {
+              // O is normalised by the fp32 sum plus the rounding error of the
+              // largest P of this half-block: in a peaked row the dominant
+              // weight's rounding would otherwise reach O undivided, while the
+              // other elements' rounding errors average out.  LSE uses the sum.
+              const float top = ex2_approx(fmaf(hmax, sl2, -m));
+              sum_r += __bfloat162float(__float2bfloat16_rn(top)) - top;
+            }
+          }
+          if (t) {
+            m1 = m;
+            l1 = l1 * alpha + sum_x;
+            r1 = r1 * alpha + sum_r;
+          } else {
+            m0 = m;
+            l0 = l0 * alpha + sum_x;
+            r0 = r0 * alpha + sum_r;
+          }
+          // Conditional rescale of this half of the running output (v4
+          // pseudo-code panel: "if need_rescale(m, m_new): acc *= exp(m -
+          // m_new)").  PV_t(j-1) is complete: its commit precedes S_t(j)'s;
+          // PV_t(j) waits for this block's signal.
+          if (j > 0 && __any_sync(0xffffffffu, need)) {
+            const uint32_t tO = t_lane + C::col_o(t) + (D / 2) * hf;
+            uint32_t orr[D / 64][32];
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) tmem_ld32(tO + 32 * c, orr[c]);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) tmem_ld_wait(orr[c]);
+            const uint64_t alpha2 = f2(alpha, alpha);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+#pragma unroll
+              for (int u = 0; u < 32; u += 2) {
+                float a, b;
+                f2_split(fmul2(f2(__uint_as_float(orr[c][u]), __uint_as_float(orr[c][u + 1])),
+                               alpha2),
+                         a, b);
+                orr[c][u] = __float_as_uint(a);
+                orr[c][u + 1] = __float_as_uint(b);
+              }
+              tmem_st32(tO + 32 * c, orr[c]);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(C::kPFull + t));
+        }
+        // tile 0 is done after block n0 - 1: its epilogue runs while the
+        // tensor core works on tile 1's next block
+        if (it.n1 > 0 && j == it.n0 - 1) epilogue(0);
+      }
+      if (it.n1 == 0) epilogue(0);
+      else epilogue(1);
+    }
+    tc_fence_before();
+    }
   }
 
   __syncthreads();
