@@ -287,7 +287,11 @@ __global__ void __launch_bounds__(384, 1)
     }
     } else if (warp == 8) {
     // ------------------------------------------------------------- MMA issue
-    if (lane == 0) {
+    // The whole warp runs this loop (waits included) and one elected lane
+    // issues the MMAs and commits: a converged warp issues faster than a
+    // lone divergent lane.
+    {
+      const uint32_t leader = elect_one();
       uint32_t slot = 0, phase = 0, q_phase = 0, p_phase[2] = {0, 0};
       bool ok = true;
       auto advance = [&]() {
@@ -306,14 +310,14 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::kHalfBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + C::col_s(t), qd + off, kd + off, C::kIdescS, kk > 0);
+          mma_ss_if(leader, tmem + C::col_s(t), qd + off, kd + off, C::kIdescS, kk > 0);
         }
       };
       auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
         const uint64_t vd = vdesc0 + ((sbase + C::kKVOff + vslot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk) {
-          mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, vd + kk * (2048 >> 4),
+          mma_ts_if(leader, tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, vd + kk * (2048 >> 4),
                  C::kIdescO, (acc || kk > 0) ? 1u : 0u);
         }
       };
@@ -336,13 +340,13 @@ __global__ void __launch_bounds__(384, 1)
         if (!(ok = wait_bar(bar(C::kKVFull + ks), kph, abort_flag, p.status))) break;
         tc_fence_after();
         issue_s(0, ks);
-        mma_commit(bar(C::kSFull + 0));
+        mma_commit_if(leader, bar(C::kSFull + 0));
         if (it.n1 > 0) {
           issue_s(1, ks);
-          mma_commit(bar(C::kSFull + 1));
+          mma_commit_if(leader, bar(C::kSFull + 1));
         }
-        mma_commit(bar(C::kKVEmpty + ks));
-        if (n_max == 1) mma_commit(bar(C::kQEmpty));
+        mma_commit_if(leader, bar(C::kKVEmpty + ks));
+        if (n_max == 1) mma_commit_if(leader, bar(C::kQEmpty));
         // PV0(0) (tile 0 always has at least one block)
         if (!(ok = wait_bar(bar(C::kKVFull + vs), vph, abort_flag, p.status))) break;
         if (!(ok = wait_bar(bar(C::kPFull + 0), p_phase[0], abort_flag, p.status))) break;
@@ -362,9 +366,9 @@ __global__ void __launch_bounds__(384, 1)
           // tile 0: S0(j+1), or the end of tile 0 (PV0(n0-1) is already queued)
           if (j + 1 < it.n0) {
             issue_s(0, ks);
-            mma_commit(bar(C::kSFull + 0));
+            mma_commit_if(leader, bar(C::kSFull + 0));
           } else if (j + 1 == it.n0) {
-            mma_commit(bar(C::kOFull + 0));
+            mma_commit_if(leader, bar(C::kOFull + 0));
           }
           // tile 1: PV1(j)
           if (j < it.n1) {
@@ -373,7 +377,7 @@ __global__ void __launch_bounds__(384, 1)
             tc_fence_after();
             issue_pv(1, vs, j > 0);
           }
-          mma_commit(bar(C::kKVEmpty + vs));  // V_j read by PV0(j) and PV1(j)
+          mma_commit_if(leader, bar(C::kKVEmpty + vs));  // V_j read by PV0(j) and PV1(j)
           uint32_t nvs = 0;
           if (more) {  // V_{j+1}: checked now, before S1's MMAs fill the queue
             nvs = slot;
@@ -384,9 +388,9 @@ __global__ void __launch_bounds__(384, 1)
           // tile 1: S1(j+1), or the end of tile 1
           if (j + 1 < it.n1) {
             issue_s(1, ks);
-            mma_commit(bar(C::kSFull + 1));
+            mma_commit_if(leader, bar(C::kSFull + 1));
           } else if (j + 1 == it.n1) {
-            mma_commit(bar(C::kOFull + 1));
+            mma_commit_if(leader, bar(C::kOFull + 1));
           }
           if (more) {
             // tile 0: PV0(j+1)
@@ -396,14 +400,14 @@ __global__ void __launch_bounds__(384, 1)
               tc_fence_after();
               issue_pv(0, nvs, true);
             }
-            mma_commit(bar(C::kKVEmpty + ks));  // K_{j+1} read by S0(j+1) and S1(j+1)
-            if (j + 2 == n_max) mma_commit(bar(C::kQEmpty));
+            mma_commit_if(leader, bar(C::kKVEmpty + ks));  // K_{j+1} read by S0(j+1) and S1(j+1)
+            if (j + 2 == n_max) mma_commit_if(leader, bar(C::kQEmpty));
             vs = nvs;
           }
         }
       }
       // Drain: all issued MMAs complete before tensor memory is freed.
-      mma_commit(bar(C::kDrain));
+      mma_commit_if(leader, bar(C::kDrain));
       wait_drain(bar(C::kDrain), 0);
     }
     }
