@@ -357,142 +357,6 @@ def run_ours(args, w):
         del pipe
 
     if rank != 0:
-        return 0
-    q, k, v = make_workload_inputs(w)
-    BH = w.B * w.H
-    tiles = (w.N + 127) // 128
-    oracle_sample_step(w, q, k, v, 0, BH, tiles)  # fp64 head copies, untimed
-    for i in range(args.warmup):
-        oracle_sample_step(w, q, k, v, i, BH, tiles)
-    flops = 0.0
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        flops += oracle_sample_step(w, q, k, v, args.warmup + i, BH, tiles)
-    dt = time.perf_counter() - t0
-    value = flops / dt / 1e12
-    line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(w.describe(), sample="128 query rows of one head per step"),
-        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cpu_cores(),
-                         "kind": "oracle",
-                         "sample": f"each step: 128 consecutive query rows of one head of "
-                                   f"{w.name} (fp64 C oracle, {cpu_cores()} threads)"},
-        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
-                "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line), flush=True)
-    return 0
-
-
-_ref_heads = {}
-
-
-def oracle_sample_step(w, q, k, v, i, BH, tiles):
-    """One reference step: 128 consecutive query rows of one head (cycling
-    over up to 8 heads whose fp64 copies are made before timing starts)."""
-    import numpy as np
-    import oracle
-    if not _ref_heads:
-        for h in range(min(8, BH)):
-            _ref_heads[h] = [oracle._as_f64(x.reshape(BH, 1, w.N, w.d)[h:h + 1].reshape(
-                1, 1, w.N, w.d)) for x in (q, k, v)]
-    sub = _ref_heads[i % len(_ref_heads)]
-    tile = (i * 3) % tiles
-    lo, hi = tile * 128, min(w.N, tile * 128 + 128)
-    rows = np.arange(lo, hi, dtype=np.int64)
-    keys = (rows + 1) if w.causal else np.full_like(rows, w.N)
-    oracle.attn_fwd(*sub, w.causal, w.scale, rows=rows, nthreads=cpu_cores())
-    return float(np.sum(4.0 * keys * w.d))
-
-
-def run_ours(args, w):
-    import torch
-
-    import exact_attention_forward_07_gb300 as fa
-
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
-    torch.cuda.set_device(dev)
-    q_h, k_h, v_h = make_workload_inputs(w)
-    q, k, v = (x.to(dev) for x in (q_h, k_h, v_h))
-    o = torch.empty_like(q)
-    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
-    call = fa.fa_fwd if w.dtype == "bf16" else fa.fa_fwd_fp16
-    stream = torch.cuda.current_stream(dev)
-    flops = w.flops()
-
-    for _ in range(args.warmup):
-        call(q, k, v, o, lse, causal=w.causal, stream=stream)
-    torch.cuda.synchronize(dev)
-    status = fa.fa_get_status(stream)
-    if status != 0:
-        raise RuntimeError(f"kernel status {status}: {fa.fa_strerror(status)}")
-
-    sampler = ClockSampler(dev.index if dev.index is not None else 0)
-    sampler.start()
-    time.sleep(0.25)
-    # ---------------------------------------------------------- timed region
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        call(q, k, v, o, lse, causal=w.causal, stream=stream)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    # ------------------------------------------------------------------------
-    clocks = sampler.stop()
-    ms_local = ev0.elapsed_time(ev1)
-    value, ms_total = job_throughput(flops, args.steps, ms_local, world)
-    ms_step = ms_total / args.steps
-    kernel_tflops = flops / (ms_local / args.steps * 1e-3) / 1e12
-    status = fa.fa_get_status(stream)
-    if status != 0:
-        raise RuntimeError(f"kernel status {status}: {fa.fa_strerror(status)}")
-
-    # ------------------------------------------------ end to end, host buffers
-    e2e = None
-    if not args.no_e2e:
-        pin = [x.pin_memory() for x in (q_h, k_h, v_h)]
-        o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        n_e2e = max(1, min(args.steps, args.e2e_steps))
-
-        def e2e_step():
-            q.copy_(pin[0], non_blocking=True)
-            k.copy_(pin[1], non_blocking=True)
-            v.copy_(pin[2], non_blocking=True)
-            call(q, k, v, o, lse, causal=w.causal, stream=stream)
-            o_h.copy_(o, non_blocking=True)
-            lse_h.copy_(lse, non_blocking=True)
-
-        for _ in range(min(3, args.warmup) or 1):
-            e2e_step()
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        ev0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier(world)
-        e2e_value, e2e_ms = job_throughput(flops, n_e2e, ev0.elapsed_time(ev1), world)
-        h2d = sum(x.numel() * x.element_size() for x in pin)
-        d2h = o_h.numel() * o_h.element_size() + lse_h.numel() * lse_h.element_size()
-        e2e = {"value": e2e_value, "unit": "TFLOPS",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
-               "ms_per_step": e2e_ms / n_e2e}
-
-    if rank != 0:
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()
@@ -542,7 +406,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--e2e-chunks", type=int, default=4)
+    ap.add_argument("--e2e-chunks", type=int, default=8)
     ap.add_argument("--cpu-heads", type=int, default=16)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

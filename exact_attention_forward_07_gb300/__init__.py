@@ -183,11 +183,12 @@ class HostPipeline:
     """Forward on pinned host buffers, pipelined over chunks of heads.
 
     Every (batch, head) is independent, so the [B*H, N, d] tensors are cut
-    into chunks of heads; chunk c's host->device copy, chunk c-1's forward
-    and chunk c-2's device->host copy run on different streams (and copy
-    engines) at the same time.  Device staging buffers for `depth` chunks
-    are allocated once, here; each call copies, computes (fa_fwd /
-    fa_fwd_fp16 through the C ABI) and copies back, then synchronises.
+    into chunks of heads.  Three in-order streams, one per engine: host ->
+    device copies, forwards (fa_fwd / fa_fwd_fp16 through the C ABI) and
+    device -> host copies, chained per chunk by events, so chunk c+1 loads
+    while chunk c computes and chunk c-1 drains.  Device staging buffers for
+    `depth` chunks are allocated once, here; each call synchronises at the
+    end.
     """
 
     def __init__(self, B, H, N, d, dtype, device=None, chunks=4, depth=3):
@@ -206,10 +207,9 @@ class HostPipeline:
             self.bufs.append(dict(q=mk(), k=mk(), v=mk(), o=mk(),
                                   lse=torch.empty((width, 1, N), dtype=torch.float32,
                                                   device=self.device)))
-        self.h2d = [torch.cuda.Stream(self.device) for _ in range(self.depth)]
-        self.comp = [torch.cuda.Stream(self.device) for _ in range(self.depth)]
-        self.d2h = [torch.cuda.Stream(self.device) for _ in range(self.depth)]
-        self.free = [None] * self.depth
+        self.s_in = torch.cuda.Stream(self.device)
+        self.s_cp = torch.cuda.Stream(self.device)
+        self.s_out = torch.cuda.Stream(self.device)
 
     def __call__(self, q, k, v, o, lse, causal=False, scale=None):
         """q, k, v, o: pinned CPU [B,H,N,d]; lse: pinned CPU [B,H,N] fp32."""
@@ -218,30 +218,29 @@ class HostPipeline:
         qf, kf, vf, of = (x.view(bh, 1, N, d) for x in (q, k, v, o))
         lf = lse.view(bh, 1, N)
         fn = fa_fwd if self.dtype == torch.bfloat16 else fa_fwd_fp16
+        free = [None] * self.depth  # buffer i drained to the host
         for c in range(self.nchunks):
             a, b = self.bounds[c], self.bounds[c + 1]
             n = b - a
             i = c % self.depth
             buf = self.bufs[i]
-            s_in, s_cp, s_out = self.h2d[i], self.comp[i], self.d2h[i]
-            if self.free[i] is not None:
-                s_in.wait_event(self.free[i])
-            with torch.cuda.stream(s_in):
+            if free[i] is not None:
+                self.s_in.wait_event(free[i])
+            with torch.cuda.stream(self.s_in):
                 for name, src in (("q", qf), ("k", kf), ("v", vf)):
                     buf[name][:n].copy_(src[a:b], non_blocking=True)
                 loaded = torch.cuda.Event()
-                loaded.record(s_in)
-            s_cp.wait_event(loaded)
-            with torch.cuda.stream(s_cp):
+                loaded.record(self.s_in)
+            self.s_cp.wait_event(loaded)
+            with torch.cuda.stream(self.s_cp):
                 fn(buf["q"][:n], buf["k"][:n], buf["v"][:n], buf["o"][:n], buf["lse"][:n],
-                   causal=causal, scale=scale, stream=s_cp)
+                   causal=causal, scale=scale, stream=self.s_cp)
                 done = torch.cuda.Event()
-                done.record(s_cp)
-            s_out.wait_event(done)
-            with torch.cuda.stream(s_out):
+                done.record(self.s_cp)
+            self.s_out.wait_event(done)
+            with torch.cuda.stream(self.s_out):
                 of[a:b].copy_(buf["o"][:n], non_blocking=True)
                 lf[a:b].copy_(buf["lse"][:n], non_blocking=True)
-                self.free[i] = torch.cuda.Event()
-                self.free[i].record(s_out)
-        for s in self.d2h:
-            s.synchronize()
+                free[i] = torch.cuda.Event()
+                free[i].record(self.s_out)
+        self.s_out.synchronize()
