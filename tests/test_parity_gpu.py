@@ -239,3 +239,17 @@ def test_host_pipeline_matches_oracle(chunks, depth):
         assert fa().fa_get_status() == 0
         o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 1.0 / math.sqrt(d))
         assert_close(o.float().numpy(), lse.numpy(), o_ref, lse_ref, f"pipeline {chunks}/{depth}")
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_parity_maximum_sequence_length(causal):
+    """N = FA_MAX_N (2^20), the longest sequence the boundary accepts: the
+    index arithmetic over 8192 Q tiles and 8192 K/V blocks, checked on
+    sampled rows (first/last rows, tile boundaries, middle, random)."""
+    N, d = fa().FA_MAX_N, 128
+    q, k, v = make_qkv(1, 1, N, d, torch.bfloat16, seed=50)
+    o, lse = run_gpu(q, k, v, causal)
+    rows = sample_rows(1, 1, N, n_random=8, seed=51)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 1.0 / math.sqrt(d), rows=rows)
+    assert_close(o.reshape(N, d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, f"N=2^20 causal={causal}")
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
