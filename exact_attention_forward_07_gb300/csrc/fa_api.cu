@@ -22,8 +22,8 @@ struct DeviceState {
   int err = FA_OK;  // FA_ERR_DEVICE / FA_ERR_CUDA if the device is unusable
   int sm_count = 0;
   unsigned *status = nullptr;  // device address of g_fa_status
-  std::once_flag attr_once[8];
-  int attr_err[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  std::once_flag attr_once[4];
+  int attr_err[4] = {0, 0, 0, 0};
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -188,15 +188,10 @@ int fwd_common(bool bf16, const void *q, const void *k, const void *v, void *o, 
   // Softmax organisation (measured on GB300): the column-split form for
   // d = 128 (3-5 % faster on every d = 128 workload, causal or not), one
   // warpgroup per Q tile for d = 64, where the split form was 2 % slower.
-  const bool split = (d == 128);
 #define FA_LAUNCH(DD, BB, SS, SLOT) \
   launch<DD, BB, SS>(*ds, SLOT, q, k, v, o, lse, BH, N, causal, scale, thr, st)
-  if (d == 64) {
-    if (bf16) return split ? FA_LAUNCH(64, true, true, 0) : FA_LAUNCH(64, true, false, 1);
-    return split ? FA_LAUNCH(64, false, true, 2) : FA_LAUNCH(64, false, false, 3);
-  }
-  if (bf16) return split ? FA_LAUNCH(128, true, true, 4) : FA_LAUNCH(128, true, false, 5);
-  return split ? FA_LAUNCH(128, false, true, 6) : FA_LAUNCH(128, false, false, 7);
+  if (d == 64) return bf16 ? FA_LAUNCH(64, true, false, 0) : FA_LAUNCH(64, false, false, 1);
+  return bf16 ? FA_LAUNCH(128, true, true, 2) : FA_LAUNCH(128, false, true, 3);
 #undef FA_LAUNCH
 }
 

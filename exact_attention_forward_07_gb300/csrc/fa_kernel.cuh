@@ -184,6 +184,39 @@ __device__ __forceinline__ uint64_t unpack2(uint32_t v) {
   }
 }
 
+// Stores a 128-byte segment of each of a warp's 32 rows (8 chunks of 16 B
+// per lane, lane = row) so that every store instruction writes whole 128-byte
+// segments: within each group of 8 lanes an 8x8 transpose of the 16-byte
+// chunks (three xor-shuffle stages) leaves lane i of the group holding chunk
+// i of the group's 8 rows.  Row r of the warp is at row0 + r * stride bytes;
+// rows r >= rows_valid are not written.
+__device__ __forceinline__ void store_rows_128B(uint4 (&v)[8], uint8_t *row0, size_t stride,
+                                                int rows_valid, uint32_t lane) {
+#pragma unroll
+  for (int k = 4; k >= 1; k >>= 1) {
+    const bool hi = (lane & k) != 0;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      if (c & k) continue;
+      const uint4 send = hi ? v[c] : v[c | k];
+      uint4 recv;
+      recv.x = __shfl_xor_sync(0xffffffffu, send.x, k);
+      recv.y = __shfl_xor_sync(0xffffffffu, send.y, k);
+      recv.z = __shfl_xor_sync(0xffffffffu, send.z, k);
+      recv.w = __shfl_xor_sync(0xffffffffu, send.w, k);
+      if (hi) v[c] = recv;
+      else v[c | k] = recv;
+    }
+  }
+  const int g = static_cast<int>(lane >> 3), i = static_cast<int>(lane & 7);
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const int row = 8 * g + r;
+    if (row < rows_valid)
+      *reinterpret_cast<uint4 *>(row0 + static_cast<size_t>(row) * stride + 16 * i) = v[r];
+  }
+}
+
 template <int D, bool BF16, bool SPLIT>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -553,26 +586,33 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t inv_l2 = f2(inv_l, inv_l);
       const bool live = q_idx < p.N;
       const size_t row_off = (static_cast<size_t>(it.bh) * p.N + q_idx);
-      uint4 *orow = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + row_off * D);
+      // this warp's first row; rows are D * 2 bytes apart
+      uint8_t *orow0 = reinterpret_cast<uint8_t *>(
+          static_cast<uint16_t *>(p.o) + (row_off - lane) * D);
+      const int rows_valid = p.N - (q_idx - static_cast<int>(lane));
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t orr[32];
-        tmem_ld32(tO + 32 * c, orr);
-        tmem_ld_wait(orr);
-        uint32_t pk16[16];
+      for (int half = 0; half < D / 64; ++half) {  // 64 columns = 128 bytes per row
+        uint4 v8[8];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          float a, b;
-          f2_split(fmul2(f2(__uint_as_float(orr[2 * u]), __uint_as_float(orr[2 * u + 1])), inv_l2),
-                   a, b);
-          pk16[u] = pack2<BF16>(a, b);
-        }
-        if (live) {
+        for (int c = 0; c < 2; ++c) {
+          uint32_t orr[32];
+          tmem_ld32(tO + 64 * half + 32 * c, orr);
+          tmem_ld_wait(orr);
+          uint32_t pk16[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            float a, b;
+            f2_split(fmul2(f2(__uint_as_float(orr[2 * u]), __uint_as_float(orr[2 * u + 1])),
+                           inv_l2),
+                     a, b);
+            pk16[u] = pack2<BF16>(a, b);
+          }
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            orow[c * 4 + u] = make_uint4(pk16[4 * u], pk16[4 * u + 1], pk16[4 * u + 2],
-                                         pk16[4 * u + 3]);
+            v8[c * 4 + u] = make_uint4(pk16[4 * u], pk16[4 * u + 1], pk16[4 * u + 2],
+                                       pk16[4 * u + 3]);
         }
+        store_rows_128B(v8, orow0 + 128 * half, static_cast<size_t>(D) * 2, rows_valid, lane);
       }
       if (live) p.lse[row_off] = (m + lg2_approx(l)) * 0.6931471805599453f;
     }
@@ -630,11 +670,11 @@ __global__ void __launch_bounds__(384, 1)
         const int q_idx = (it.qt0 + t) * 128 + row;
         const bool live = q_idx < p.N;
         const size_t row_off = (static_cast<size_t>(it.bh) * p.N + q_idx);
-        uint4 *orow = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + row_off * D +
-                                                (D / 2) * hf);
         const uint32_t tO = t_lane + C::col_o(t) + (D / 2) * hf;
+        static_assert(!SPLIT || D == 128, "column split stores 64 columns (128 bytes) per warp");
+        uint4 v8[8];
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t orr[32];
           tmem_ld32(tO + 32 * c, orr);
           tmem_ld_wait(orr);
@@ -647,13 +687,17 @@ __global__ void __launch_bounds__(384, 1)
                      a, b);
             pk16[u] = pack2<BF16>(a, b);
           }
-          if (live) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              orow[c * 4 + u] = make_uint4(pk16[4 * u], pk16[4 * u + 1], pk16[4 * u + 2],
-                                           pk16[4 * u + 3]);
-          }
+          for (int u = 0; u < 4; ++u)
+            v8[c * 4 + u] = make_uint4(pk16[4 * u], pk16[4 * u + 1], pk16[4 * u + 2],
+                                       pk16[4 * u + 3]);
         }
+        // this warp's first row, its half of the columns; rows D * 2 bytes apart
+        store_rows_128B(v8,
+                        reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.o) +
+                                                    (row_off - lane) * D + (D / 2) * hf),
+                        static_cast<size_t>(D) * 2, p.N - (q_idx - static_cast<int>(lane)),
+                        lane);
         if (live && hf == 0)
           p.lse[row_off] = ((t ? m1 : m0) + lg2_approx(lsum)) * 0.6931471805599453f;
       };
