@@ -75,8 +75,9 @@ struct Cfg {
   static constexpr int kKVOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
   // barrier indices
-  static constexpr int kQFull = 0, kQEmpty = 1, kKVFull = 2, kKVEmpty = 2 + kStages;
-  static constexpr int kSFull = 2 + 2 * kStages, kPFull = kSFull + 2, kOFull = kPFull + 2;
+  // per Q tile: kQFull + t, kQEmpty + t
+  static constexpr int kQFull = 0, kQEmpty = 2, kKVFull = 4, kKVEmpty = 4 + kStages;
+  static constexpr int kSFull = 4 + 2 * kStages, kPFull = kSFull + 2, kOFull = kPFull + 2;
   static constexpr int kDrain = kOFull + 2;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
@@ -241,8 +242,10 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(C::kKVFull + i), 1);
       mbar_init(bar(C::kKVEmpty + i), 1);
     }
-    mbar_init(bar(C::kQFull), 1);
-    mbar_init(bar(C::kQEmpty), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::kQFull + t), 1);
+      mbar_init(bar(C::kQEmpty + t), 1);
+    }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::kSFull + t), 1);
       mbar_init(bar(C::kPFull + t), SPLIT ? 8 : 4);  // one arrive per softmax warp
@@ -275,22 +278,27 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
-      uint32_t slot = 0, phase = 0, q_phase = 0;
-      uint32_t kv_loads = 0, q_loads = 0;
+      uint32_t slot = 0, phase = 0, q_phase[2] = {0, 0};
+      uint32_t kv_loads = 0, q_loads[2] = {0, 0};
       bool ok = true;
       for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_items; ++round) {
         const int item = round_item(round, p);
         if (item < 0) continue;
         const Item it = decode_item(item, p);
-        if (!(ok = wait_bar(bar(C::kQEmpty), q_phase ^ 1u, abort_flag, p.status))) break;
-        q_phase ^= 1u;
+        // Each Q tile's buffer is released by its own last S MMA of the
+        // previous item, so tile 0's next tile can load while tile 1 still
+        // computes.
         const int nq = it.n1 > 0 ? 2 : 1;
-        mbar_arrive_expect_tx(bar(C::kQFull), nq * C::kTileBytes);
-        for (int t = 0; t < nq; ++t)
+        for (int t = 0; ok && t < nq; ++t) {
+          if (!(ok = wait_bar(bar(C::kQEmpty + t), q_phase[t] ^ 1u, abort_flag, p.status))) break;
+          q_phase[t] ^= 1u;
+          mbar_arrive_expect_tx(bar(C::kQFull + t), C::kTileBytes);
           for (int h = 0; h < D / 64; ++h)
             tma_load_3d(sbase + C::kQOff + t * C::kTileBytes + h * C::kHalfBytes, &tm_q,
-                        bar(C::kQFull), h * 64, (it.qt0 + t) * 128, it.bh, pol_q);
-        ++q_loads;
+                        bar(C::kQFull + t), h * 64, (it.qt0 + t) * 128, it.bh, pol_q);
+          ++q_loads[t];
+        }
+        if (!ok) break;
         const int n_max = it.n0 > it.n1 ? it.n0 : it.n1;
         for (int j = 0; ok && j < n_max; ++j) {
           for (int kv = 0; kv < 2; ++kv) {
@@ -316,7 +324,8 @@ __global__ void __launch_bounds__(384, 1)
           wait_drain(bar(C::kKVFull + s), (cnt - 1) & 1u);
         }
       }
-      if (q_loads) wait_drain(bar(C::kQFull), (q_loads - 1) & 1u);
+      for (int t = 0; t < 2; ++t)
+        if (q_loads[t]) wait_drain(bar(C::kQFull + t), (q_loads[t] - 1) & 1u);
     }
     } else if (warp == 8) {
     // ------------------------------------------------------------- MMA issue
@@ -325,7 +334,7 @@ __global__ void __launch_bounds__(384, 1)
     // lone divergent lane.
     {
       const uint32_t leader = elect_one();
-      uint32_t slot = 0, phase = 0, q_phase = 0, p_phase[2] = {0, 0};
+      uint32_t slot = 0, phase = 0, q_phase[2] = {0, 0}, p_phase[2] = {0, 0};
       bool ok = true;
       auto advance = [&]() {
         if (++slot == C::kStages) {
@@ -363,8 +372,8 @@ __global__ void __launch_bounds__(384, 1)
         if (item < 0) continue;
         const Item it = decode_item(item, p);
         const int n_max = it.n0 > it.n1 ? it.n0 : it.n1;
-        if (!(ok = wait_bar(bar(C::kQFull), q_phase, abort_flag, p.status))) break;
-        q_phase ^= 1u;
+        if (!(ok = wait_bar(bar(C::kQFull + 0), q_phase[0], abort_flag, p.status))) break;
+        q_phase[0] ^= 1u;
         // K_0 and V_0 positions in the ring
         uint32_t ks = slot, kph = phase;
         advance();
@@ -374,12 +383,16 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         issue_s(0, ks);
         mma_commit_if(leader, bar(C::kSFull + 0));
+        if (it.n0 == 1) mma_commit_if(leader, bar(C::kQEmpty + 0));
         if (it.n1 > 0) {
+          if (!(ok = wait_bar(bar(C::kQFull + 1), q_phase[1], abort_flag, p.status))) break;
+          q_phase[1] ^= 1u;
+          tc_fence_after();
           issue_s(1, ks);
           mma_commit_if(leader, bar(C::kSFull + 1));
+          if (it.n1 == 1) mma_commit_if(leader, bar(C::kQEmpty + 1));
         }
         mma_commit_if(leader, bar(C::kKVEmpty + ks));
-        if (n_max == 1) mma_commit_if(leader, bar(C::kQEmpty));
         // PV0(0) (tile 0 always has at least one block)
         if (!(ok = wait_bar(bar(C::kKVFull + vs), vph, abort_flag, p.status))) break;
         if (!(ok = wait_bar(bar(C::kPFull + 0), p_phase[0], abort_flag, p.status))) break;
@@ -400,6 +413,7 @@ __global__ void __launch_bounds__(384, 1)
           if (j + 1 < it.n0) {
             issue_s(0, ks);
             mma_commit_if(leader, bar(C::kSFull + 0));
+            if (j + 2 == it.n0) mma_commit_if(leader, bar(C::kQEmpty + 0));  // last S0
           } else if (j + 1 == it.n0) {
             mma_commit_if(leader, bar(C::kOFull + 0));
           }
@@ -422,6 +436,7 @@ __global__ void __launch_bounds__(384, 1)
           if (j + 1 < it.n1) {
             issue_s(1, ks);
             mma_commit_if(leader, bar(C::kSFull + 1));
+            if (j + 2 == it.n1) mma_commit_if(leader, bar(C::kQEmpty + 1));  // last S1
           } else if (j + 1 == it.n1) {
             mma_commit_if(leader, bar(C::kOFull + 1));
           }
@@ -434,7 +449,6 @@ __global__ void __launch_bounds__(384, 1)
               issue_pv(0, nvs, true);
             }
             mma_commit_if(leader, bar(C::kKVEmpty + ks));  // K_{j+1} read by S0(j+1) and S1(j+1)
-            if (j + 2 == n_max) mma_commit_if(leader, bar(C::kQEmpty));
             vs = nvs;
           }
         }
