@@ -22,6 +22,7 @@ struct DeviceState {
   int err = FA_OK;  // FA_ERR_DEVICE / FA_ERR_CUDA if the device is unusable
   int sm_count = 0;
   unsigned *status = nullptr;  // device address of g_fa_status
+  cudaMemPool_t pool = nullptr;  // stream-ordered scratch for split items (none: no split)
   std::once_flag attr_once[4];
   int attr_err[4] = {0, 0, 0, 0};
 };
@@ -83,6 +84,22 @@ int device_state(DeviceState **out) {
       return;
     }
     s.status = static_cast<unsigned *>(addr);
+    // A private memory pool that keeps what it has allocated, so the split
+    // schedule's scratch memory costs no device allocation after the first
+    // call.  Without it the library runs every item whole.
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    if (cudaMemPoolCreate(&s.pool, &props) == cudaSuccess) {
+      uint64_t keep = UINT64_MAX;
+      cudaMemPoolSetAttribute(s.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    } else {
+      s.pool = nullptr;
+      cudaGetLastError();
+    }
   });
   if (s.err != FA_OK) return s.err;
   *out = &s;
@@ -147,9 +164,57 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.rescale_thr = thr;
 
-  const int grid = p.n_items < ds.sm_count ? p.n_items : ds.sm_count;
+  // Wave-tail split.  With G persistent CTAs, the last round holds
+  // R = n_items mod G items and leaves G - R SMs idle; when R <= G / 2 each
+  // of those items is cut into k = min(G / R, kMaxSplit, n_qtiles) pieces
+  // along the keys, so the last round takes about 1/k of the time.  The
+  // pieces' results go to scratch memory (stream-ordered, from the
+  // library's pool) and are merged by the last piece of each item.
+  p.n_units = p.n_items;
+  p.split_first = p.n_items;
+  p.split_k = 1;
+  p.part_o = nullptr;
+  p.part_st = nullptr;
+  p.part_cnt = nullptr;
+  void *scratch = nullptr;
+  if (SPLIT && !causal && ds.pool != nullptr) {
+    const int G = ds.sm_count;
+    const int R = p.n_items % G;
+    int k = R > 0 ? G / R : 0;
+    if (k > fa::kMaxSplit) k = fa::kMaxSplit;
+    if (k > p.n_qtiles) k = p.n_qtiles;
+    if (k >= 2) {
+      const size_t pieces = static_cast<size_t>(R) * k;
+      const size_t bytes_o = pieces * 256 * D * sizeof(float);
+      const size_t bytes_st = (pieces * 256 * 3 * sizeof(float) + 255) & ~static_cast<size_t>(255);
+      const size_t bytes_cnt = static_cast<size_t>(R) * sizeof(unsigned);
+      // a failed scratch allocation only means no split (its error is cleared)
+      if (cudaMallocFromPoolAsync(&scratch, bytes_o + bytes_st + bytes_cnt, ds.pool, stream) !=
+          cudaSuccess) {
+        scratch = nullptr;
+        cudaGetLastError();
+      } else {
+        uint8_t *base = static_cast<uint8_t *>(scratch);
+        if (cudaMemsetAsync(base + bytes_o + bytes_st, 0, bytes_cnt, stream) == cudaSuccess) {
+          p.split_first = p.n_items - R;
+          p.split_k = k;
+          p.n_units = p.split_first + R * k;
+          p.part_o = reinterpret_cast<float4 *>(base);
+          p.part_st = reinterpret_cast<float *>(base + bytes_o);
+          p.part_cnt = reinterpret_cast<unsigned *>(base + bytes_o + bytes_st);
+        } else {
+          cudaGetLastError();
+          cudaFreeAsync(scratch, stream);
+          scratch = nullptr;
+        }
+      }
+    }
+  }
+
+  const int grid = p.n_units < ds.sm_count ? p.n_units : ds.sm_count;
   kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
   cudaError_t e = cudaGetLastError();
+  if (scratch != nullptr) cudaFreeAsync(scratch, stream);
   if (e != cudaSuccess) {
     if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
       return FA_ERR_DEVICE;

@@ -48,6 +48,7 @@
 namespace fa {
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s without progress
+constexpr int kMaxSplit = 4;                     // most pieces a split item is cut into
 constexpr uint32_t kStatusTimeout = 1u;
 
 struct Params {
@@ -62,6 +63,17 @@ struct Params {
   int causal;
   float scale_log2;  // scale * log2(e)
   float rescale_thr; // rescale O only when the running max grows by more than this (log2 units)
+  // Wave-tail split (non-causal, column-split kernel only): the items from
+  // split_first on (those of the last, partial round of the persistent
+  // grid) are cut into split_k pieces along the key blocks; each piece
+  // leaves its O (normalised by its own sum) and row statistics in scratch
+  // memory, and the last piece of an item to finish merges them.
+  int n_units;          // work units: split_first + (n_items - split_first) * split_k
+  int split_first;      // first split item (n_items: none)
+  int split_k;          // pieces per split item
+  float4 *part_o;       // [piece][D / 4 column groups][256 rows] fp32 x 4
+  float *part_st;       // [piece][3][256 rows]: max (log2 units), sum of P, corrected sum
+  unsigned *part_cnt;   // [split item]: pieces finished (zero before the launch)
 };
 
 template <int D, bool BF16>
@@ -80,7 +92,7 @@ struct Cfg {
   static constexpr int kSFull = 4 + 2 * kStages, kPFull = kSFull + 2, kOFull = kPFull + 2;
   static constexpr int kDrain = kOFull + 2;
   static constexpr int kNumBars = kDrain + 1;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag, merge flag
   static constexpr int kXchOff = (kMiscOff + 16 + 15) & ~15;  // softmax row exchange, 4 KB
   static constexpr int kSmemBytes = kXchOff + 2 * 2 * 2 * 128 * 4 + 1024;  // + base alignment slack
   static constexpr uint32_t kTmemCols = 512;
@@ -96,6 +108,8 @@ struct Cfg {
 
 struct Item {
   int bh, qt0, n0, n1;
+  int j0;     // first K/V block
+  int piece;  // -1: a whole item; else the global piece index
 };
 
 // Work item -> (head, first Q tile, K/V blocks for each of the two tiles).
@@ -120,7 +134,28 @@ __device__ __forceinline__ Item decode_item(int item, const Params &p) {
   return it;
 }
 
-// The item a CTA takes in a given round of the persistent loop, or -1.
+// Work unit -> item, with the key-block range of a piece of a split item.
+// Piece c of k takes blocks [c * n / k, (c + 1) * n / k) of the n_qtiles.
+__device__ __forceinline__ Item decode_unit(int unit, const Params &p) {
+  if (unit < p.split_first) {
+    Item it = decode_item(unit, p);
+    it.j0 = 0;
+    it.piece = -1;
+    return it;
+  }
+  const int s = unit - p.split_first;
+  const int k = p.split_k;
+  const int q = s / k, c = s - q * k;
+  Item it = decode_item(p.split_first + q, p);
+  const int lo = c * p.n_qtiles / k, hi = (c + 1) * p.n_qtiles / k;
+  it.j0 = lo;
+  it.n0 = hi - lo;
+  it.n1 = it.n1 > 0 ? hi - lo : 0;
+  it.piece = s;
+  return it;
+}
+
+// The work unit a CTA takes in a given round of the persistent loop, or -1.
 // Causal rounds alternate direction so the CTA that took the heaviest item
 // of one round takes the lightest of the next.
 __device__ __forceinline__ int round_item(int round, const Params &p) {
@@ -128,7 +163,7 @@ __device__ __forceinline__ int round_item(int round, const Params &p) {
   const int off = (p.causal && (round & 1)) ? static_cast<int>(gridDim.x - 1 - blockIdx.x)
                                             : static_cast<int>(blockIdx.x);
   const int idx = base + off;
-  return idx < p.n_items ? idx : -1;
+  return idx < p.n_units ? idx : -1;
 }
 
 __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
@@ -281,10 +316,10 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t slot = 0, phase = 0, q_phase[2] = {0, 0};
       uint32_t kv_loads = 0, q_loads[2] = {0, 0};
       bool ok = true;
-      for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_items; ++round) {
+      for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_units; ++round) {
         const int item = round_item(round, p);
         if (item < 0) continue;
-        const Item it = decode_item(item, p);
+        const Item it = decode_unit(item, p);
         // Each Q tile's buffer is released by its own last S MMA of the
         // previous item, so tile 0's next tile can load while tile 1 still
         // computes.
@@ -307,7 +342,7 @@ __global__ void __launch_bounds__(384, 1)
             const CUtensorMap *m = kv ? &tm_v : &tm_k;
             for (int h = 0; h < D / 64; ++h)
               tma_load_3d(sbase + C::kKVOff + slot * C::kTileBytes + h * C::kHalfBytes, m,
-                          bar(C::kKVFull + slot), h * 64, j * 128, it.bh, pol_kv);
+                          bar(C::kKVFull + slot), h * 64, (it.j0 + j) * 128, it.bh, pol_kv);
             ++kv_loads;
             if (++slot == C::kStages) {
               slot = 0;
@@ -367,10 +402,10 @@ __global__ void __launch_bounds__(384, 1)
       // of a K slot) falls right after PV0's MMAs are queued: between the end
       // of S1's issue and the start of PV0's there is then only one commit
       // and one wait, and the tensor core's short queue does not run dry.
-      for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_items; ++round) {
+      for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_units; ++round) {
         const int item = round_item(round, p);
         if (item < 0) continue;
-        const Item it = decode_item(item, p);
+        const Item it = decode_unit(item, p);
         const int n_max = it.n0 > it.n1 ? it.n0 : it.n1;
         if (!(ok = wait_bar(bar(C::kQFull + 0), q_phase[0], abort_flag, p.status))) break;
         q_phase[0] ^= 1u;
@@ -473,10 +508,10 @@ __global__ void __launch_bounds__(384, 1)
     const float sl2 = p.scale_log2;
     uint32_t s_phase = 0, o_phase = 0;
     bool ok = true;
-    for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_items; ++round) {
+    for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_units; ++round) {
       const int item = round_item(round, p);
       if (item < 0) continue;
-      const Item it = decode_item(item, p);
+      const Item it = decode_unit(item, p);
       const int n = t ? it.n1 : it.n0;
       if (n == 0) continue;
       const int qt = it.qt0 + t;
@@ -502,8 +537,8 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (c > row) s[c] = -INFINITY;
-        } else if (!p.causal && j == p.n_qtiles - 1 && (p.N & 127)) {
-          const int lim = p.N - j * 128;
+        } else if (!p.causal && it.j0 + j == p.n_qtiles - 1 && (p.N & 127)) {
+          const int lim = p.N - (it.j0 + j) * 128;
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (c >= lim) s[c] = -INFINITY;
@@ -648,16 +683,85 @@ __global__ void __launch_bounds__(384, 1)
     auto xslot = [&](uint32_t par, int h, int val) { return xch + ((par * 2 + h) * 2 + val) * 128 + row; };
     const uint32_t pair_bar = 1u + static_cast<uint32_t>(q);  // named barrier of the quadrant's two warps
     auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
+    // all eight softmax warps (named barrier 5)
+    auto softmax_sync = [&]() { asm volatile("bar.sync 5, 256;" ::: "memory"); };
+    volatile unsigned *merge_flag = reinterpret_cast<volatile unsigned *>(smem + C::kMiscOff + 8);
+    // Merge of the pieces of a split item, tile t, this thread's row and
+    // half of the columns: with M the largest of the pieces' maxima, piece
+    // c weighs r_c 2^(m_c - M) (its corrected sum) in O, and the logsumexp
+    // is M + log2(sum_c l_c 2^(m_c - M)) (in log2 units).  Reads go to L2
+    // (other SMs wrote the pieces).
+    auto merge = [&](const Item &it, int t) {
+      const int k = p.split_k;
+      const int first = (it.piece / k) * k;
+      const int prow_in_item = t * 128 + row;
+      float m_c[kMaxSplit], w[kMaxSplit];
+      float M = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kMaxSplit; ++c) {
+        m_c[c] = -INFINITY;
+        if (c < k) {
+          m_c[c] = __ldcg(p.part_st + static_cast<size_t>(first + c) * 3 * 256 + prow_in_item);
+          M = fmaxf(M, m_c[c]);
+        }
+      }
+      float wl = 0.f, wr = 0.f;
+#pragma unroll
+      for (int c = 0; c < kMaxSplit; ++c) {
+        w[c] = 0.f;
+        if (c < k) {
+          const float *st = p.part_st + static_cast<size_t>(first + c) * 3 * 256 + prow_in_item;
+          const float e = ex2_approx(m_c[c] - M);
+          wl += __ldcg(st + 256) * e;
+          w[c] = __ldcg(st + 512) * e;
+          wr += w[c];
+        }
+      }
+      const float inv = 1.f / wr;
+      float acc[D / 2];
+#pragma unroll
+      for (int e = 0; e < D / 2; ++e) acc[e] = 0.f;
+#pragma unroll
+      for (int c = 0; c < kMaxSplit; ++c) {
+        if (c < k) {
+          const float wc = w[c] * inv;
+          const float4 *src =
+              p.part_o + (static_cast<size_t>(first + c) * (D / 4) + (D / 8) * hf) * 256 + prow_in_item;
+#pragma unroll
+          for (int u = 0; u < D / 8; ++u) {
+            const float4 x = __ldcg(src + u * 256);
+            acc[4 * u] = fmaf(wc, x.x, acc[4 * u]);
+            acc[4 * u + 1] = fmaf(wc, x.y, acc[4 * u + 1]);
+            acc[4 * u + 2] = fmaf(wc, x.z, acc[4 * u + 2]);
+            acc[4 * u + 3] = fmaf(wc, x.w, acc[4 * u + 3]);
+          }
+        }
+      }
+      uint4 v8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v8[u] = make_uint4(pack2<BF16>(acc[8 * u], acc[8 * u + 1]),
+                           pack2<BF16>(acc[8 * u + 2], acc[8 * u + 3]),
+                           pack2<BF16>(acc[8 * u + 4], acc[8 * u + 5]),
+                           pack2<BF16>(acc[8 * u + 6], acc[8 * u + 7]));
+      const int q_idx = (it.qt0 + t) * 128 + row;
+      const size_t row_off = static_cast<size_t>(it.bh) * p.N + q_idx;
+      store_rows_128B(v8,
+                      reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.o) +
+                                                  (row_off - lane) * D + (D / 2) * hf),
+                      static_cast<size_t>(D) * 2, p.N - (q_idx - static_cast<int>(lane)), lane);
+      if (q_idx < p.N && hf == 0) p.lse[row_off] = (M + lg2_approx(wl)) * 0.6931471805599453f;
+    };
     const float sl2 = p.scale_log2;
     uint32_t s_par = 0, o_par = 0, xpar = 0;  // barrier phase bits per tile, exchange parity
     // bar.sync cannot time out, so a warp whose wait gave up (ok == false)
     // keeps walking the same sequence of blocks, doing no work but taking
     // part in every pair barrier, so its partner can never be left waiting.
     bool ok = true;
-    for (int round = 0; round * static_cast<int>(gridDim.x) < p.n_items; ++round) {
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.n_units; ++round) {
       const int item = round_item(round, p);
       if (item < 0) continue;
-      const Item it = decode_item(item, p);
+      const Item it = decode_unit(item, p);
       const int n_max = it.n0 > it.n1 ? it.n0 : it.n1;
       // per tile: running max (log2 units), this half's sums of P and of P
       // corrected for the rounding of each block's largest value
@@ -686,6 +790,33 @@ __global__ void __launch_bounds__(384, 1)
         const size_t row_off = (static_cast<size_t>(it.bh) * p.N + q_idx);
         const uint32_t tO = t_lane + C::col_o(t) + (D / 2) * hf;
         static_assert(!SPLIT || D == 128, "column split stores 64 columns (128 bytes) per warp");
+        if (it.piece >= 0) {
+          // a piece of a split item: its O normalised by its own sum (fp32)
+          // and its row statistics go to scratch memory for the merge, in a
+          // column-group-major layout so that a warp's 32 rows are 512
+          // contiguous bytes
+          const int prow = t * 128 + row;
+          float4 *dst = p.part_o + (static_cast<size_t>(it.piece) * (D / 4) + (D / 8) * hf) * 256 + prow;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t orr[32];
+            tmem_ld32(tO + 32 * c, orr);
+            tmem_ld_wait(orr);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              dst[(8 * c + u) * 256] = make_float4(__uint_as_float(orr[4 * u]) * inv_l,
+                                                   __uint_as_float(orr[4 * u + 1]) * inv_l,
+                                                   __uint_as_float(orr[4 * u + 2]) * inv_l,
+                                                   __uint_as_float(orr[4 * u + 3]) * inv_l);
+          }
+          if (hf == 0) {
+            float *st = p.part_st + static_cast<size_t>(it.piece) * 3 * 256 + prow;
+            st[0] = t ? m1 : m0;
+            st[256] = lsum;
+            st[512] = rsum;
+          }
+          return;
+        }
         uint4 v8[8];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -743,8 +874,8 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int c = 0; c < 64; ++c)
               if (c > lim) s[c] = -INFINITY;
-          } else if (!p.causal && j == p.n_qtiles - 1 && (p.N & 127)) {
-            const int lim = p.N - j * 128 - 64 * hf;
+          } else if (!p.causal && it.j0 + j == p.n_qtiles - 1 && (p.N & 127)) {
+            const int lim = p.N - (it.j0 + j) * 128 - 64 * hf;
 #pragma unroll
             for (int c = 0; c < 64; ++c)
               if (c >= lim) s[c] = -INFINITY;
@@ -850,6 +981,25 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (it.n1 == 0) epilogue(0);
       else epilogue(1);
+      if (it.piece >= 0) {
+        // The piece's results are in scratch memory: make them visible to
+        // the whole device, count the piece, and if it was the item's last
+        // one, merge all pieces of the item.  The two barriers are taken on
+        // every path.
+        __threadfence();
+        softmax_sync();
+        if (threadIdx.x == 0) {
+          unsigned last = 0;
+          if (ok)
+            last = atomicAdd(p.part_cnt + it.piece / p.split_k, 1u) ==
+                   static_cast<unsigned>(p.split_k - 1);
+          *merge_flag = last;
+        }
+        softmax_sync();
+        if (ok && *merge_flag) {
+          for (int t = 0; t < (it.n1 > 0 ? 2 : 1); ++t) merge(it, t);
+        }
+      }
     }
     tc_fence_before();
     }

@@ -142,6 +142,41 @@ def test_causal_row_zero_is_v0():
     assert np.max(np.abs(lse[:, :, 0] - s00) / np.maximum(1, np.abs(s00))) <= LSE_REL
 
 
+# Non-causal d = 128 shapes whose last round of work items is cut into key
+# pieces (the wave-tail split): k = 4 pieces with every item split, an odd
+# tile count with a ragged end, k = 3 with one block per piece, and a mix of
+# whole and split items (k = 2) on a 152-SM device.
+SPLIT_SHAPES = [
+    (1, 2, 4096, torch.bfloat16),
+    (1, 1, 4097, torch.float16),
+    (1, 5, 300, torch.bfloat16),
+    (1, 64, 2048, torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("B,H,N,dtype", SPLIT_SHAPES,
+                         ids=[f"b{b}h{h}n{n}-{str(t)[6:]}" for b, h, n, t in SPLIT_SHAPES])
+def test_parity_wave_tail_split(B, H, N, dtype):
+    q, k, v = make_qkv(B, H, N, 128, dtype, seed=60 + N + H)
+    o, lse = run_gpu(q, k, v, False)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, False, 1.0 / math.sqrt(128))
+    assert_close(o, lse, o_ref, lse_ref, f"split {B},{H},{N},{dtype}")
+
+
+def test_wave_tail_split_peaked_rows():
+    """Pieces of one row see very different maxima (K scaled x6, sorted so
+    the largest logits sit in the last piece): the merge must weigh each
+    piece by its own max and sum."""
+    B, H, N, d = 1, 3, 2048, 128
+    q, k, v = make_qkv(B, H, N, d, torch.bfloat16, seed=61, k_mult=6.0)
+    order = torch.argsort((q[0, 0].float().mean(0) @ k[0].float().transpose(-1, -2)).mean(0))
+    k = k[:, :, order].contiguous()
+    for thr in (0.0, 8.0):
+        o, lse = run_gpu(q, k, v, False, rescale_threshold=thr)
+        o_ref, lse_ref = oracle.attn_fwd(q, k, v, False, 1.0 / math.sqrt(d))
+        assert_close(o, lse, o_ref, lse_ref, f"split peaked thr={thr}")
+
+
 def test_deterministic_bitwise():
     q, k, v = make_qkv(2, 8, 1536, 128, torch.bfloat16, seed=9)
     dev = torch.device("cuda")
@@ -149,6 +184,14 @@ def test_deterministic_bitwise():
     for causal in (False, True):
         o1, l1 = fa().forward(q, k, v, causal=causal)
         o2, l2 = fa().forward(q, k, v, causal=causal)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    # split items: the merge reads the pieces in a fixed order, whichever
+    # piece finishes last
+    q, k, v = (x.to(dev) for x in make_qkv(1, 2, 4096, 128, torch.bfloat16, seed=19))
+    o1, l1 = fa().forward(q, k, v, causal=False)
+    for _ in range(3):
+        o2, l2 = fa().forward(q, k, v, causal=False)
         torch.cuda.synchronize()
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
