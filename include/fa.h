@@ -19,10 +19,18 @@
  * share N (self-attention shape).  Every pointer is a DEVICE pointer on the
  * current CUDA device.
  *
- * Ownership: the caller allocates and owns every buffer; the library
- * allocates nothing per call.  Per-device state (SM count, kernel
- * attributes, one 4-byte status word) is created on first use and lives
- * until process exit.  o and lse must not overlap q, k, v or each other.
+ * Ownership: the caller allocates and owns q, k, v, o and lse.  Non-causal
+ * d = 128 calls whose last round of work items is split along the keys (the
+ * wave-tail split: when fewer than half the SMs would have an item in the
+ * last round) take scratch memory for the pieces' partial results -- at
+ * most one piece per SM, 131 KiB each, plus 4 bytes per split item -- from
+ * a stream-ordered memory pool the library creates per device; it is
+ * returned to the pool behind the kernel on the same stream, and the pool
+ * keeps its memory, so after the first such call no device allocation
+ * happens.  If the pool cannot supply it the call runs unsplit.  Per-device
+ * state (SM count, kernel attributes, one 4-byte status word, the pool) is
+ * created on first use and lives until process exit.  o and lse must not
+ * overlap q, k, v or each other.
  *
  * Execution: asynchronous on `stream` (0 = legacy default stream); no host
  * synchronisation.  Safe to call from several host threads.
