@@ -34,7 +34,9 @@ FA_ERR_CUDA = -8
 FA_ERR_TIMEOUT = -9
 FA_ERR_ALIAS = -10
 FA_ERR_OPTION = -11
+FA_ERR_SCRATCH = -12
 FA_MAX_N = 1 << 20
+FA_NOALLOC_SCRATCH_BYTES = 16 << 20
 FA_DEFAULT_RESCALE_THRESHOLD = 8.0
 FA_MAX_RESCALE_THRESHOLD = 12.0
 
@@ -71,6 +73,8 @@ def lib():
         L.fa_fwd_ex.argtypes = [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int, ctypes.c_float,
                                 ctypes.c_int, ctypes.c_float, P]
         L.fa_fwd_ex.restype = ctypes.c_int
+        L.fa_fwd_noalloc.argtypes = L.fa_fwd_ex.argtypes
+        L.fa_fwd_noalloc.restype = ctypes.c_int
         L.fa_selftest_wait_timeout.argtypes = [I64, P, P]
         L.fa_selftest_wait_timeout.restype = ctypes.c_int
         L.fa_get_status.argtypes = [P]
@@ -154,6 +158,21 @@ def fa_fwd_ex(q, k, v, o, lse, causal=False, scale=None, rescale_threshold=None,
         raise TypeError(f"unsupported dtype {q.dtype}: use bfloat16 or float16")
     fp16 = int(q.dtype == torch.float16)
     _call("fa_fwd_ex", q, k, v, o, lse, causal, scale, stream, q.dtype,
+          extra=(fp16, float(rescale_threshold)))
+
+
+def fa_fwd_noalloc(q, k, v, o, lse, causal=False, scale=None, rescale_threshold=None,
+                   stream=None) -> None:
+    """fa_fwd_ex that never allocates device memory (its split scratch is a
+    fixed array; FaError FA_ERR_SCRATCH when a call needs more).  Calls must
+    not overlap in time."""
+    import torch
+    if rescale_threshold is None:
+        rescale_threshold = FA_DEFAULT_RESCALE_THRESHOLD
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"unsupported dtype {q.dtype}: use bfloat16 or float16")
+    fp16 = int(q.dtype == torch.float16)
+    _call("fa_fwd_noalloc", q, k, v, o, lse, causal, scale, stream, q.dtype,
           extra=(fp16, float(rescale_threshold)))
 
 

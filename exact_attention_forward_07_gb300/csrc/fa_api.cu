@@ -14,6 +14,8 @@
 namespace {
 
 __device__ unsigned g_fa_status = 0;  // per-device status word (FA_ERR_TIMEOUT source)
+// fa_fwd_noalloc's scratch: a fixed array instead of pool memory
+__device__ __align__(256) unsigned char g_fa_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
 
@@ -23,6 +25,7 @@ struct DeviceState {
   int sm_count = 0;
   unsigned *status = nullptr;  // device address of g_fa_status
   cudaMemPool_t pool = nullptr;  // stream-ordered scratch for split items (none: no split)
+  uint8_t *noalloc = nullptr;    // device address of g_fa_noalloc_scratch
   std::once_flag attr_once[4];
   int attr_err[4] = {0, 0, 0, 0};
 };
@@ -84,6 +87,14 @@ int device_state(DeviceState **out) {
       return;
     }
     s.status = static_cast<unsigned *>(addr);
+    void *scr = nullptr;
+    cudaError_t e5 = cudaGetSymbolAddress(&scr, g_fa_noalloc_scratch);
+    if (e5 != cudaSuccess) {
+      t_last_cuda_error = static_cast<int>(e5);
+      s.err = FA_ERR_CUDA;
+      return;
+    }
+    s.noalloc = static_cast<uint8_t *>(scr);
     // A private memory pool that keeps what it has allocated, so the split
     // schedule's scratch memory costs no device allocation after the first
     // call.  Without it the library runs every item whole.
@@ -134,7 +145,7 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 
 template <int D, bool BF16, bool SPLIT>
 int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *v, void *o,
-           float *lse, int64_t BH, int64_t N, int causal, float scale, float thr,
+           float *lse, int64_t BH, int64_t N, int causal, float scale, float thr, bool noalloc,
            cudaStream_t stream) {
   using C = fa::Cfg<D, BF16>;
   auto kernel = fa::fa_fwd_kernel<D, BF16, SPLIT>;
@@ -169,15 +180,17 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
   // of those items is cut into k = min(G / R, kMaxSplit, n_qtiles) pieces
   // along the keys, so the last round takes about 1/k of the time.  The
   // pieces' results go to scratch memory (stream-ordered, from the
-  // library's pool) and are merged by the last piece of each item.
+  // library's pool; for fa_fwd_noalloc, the fixed array, and a plan that
+  // does not fit it is rejected) and are merged by the last piece of each
+  // item.
   p.n_units = p.n_items;
   p.split_first = p.n_items;
   p.split_k = 1;
   p.part_o = nullptr;
   p.part_st = nullptr;
   p.part_cnt = nullptr;
-  void *scratch = nullptr;
-  if (SPLIT && !causal && ds.pool != nullptr) {
+  void *scratch = nullptr;  // pool memory to give back after the launch
+  if (SPLIT && !causal && (noalloc || ds.pool != nullptr)) {
     const int G = ds.sm_count;
     const int R = p.n_items % G;
     int k = R > 0 ? G / R : 0;
@@ -188,13 +201,19 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
       const size_t bytes_o = pieces * 256 * D * sizeof(float);
       const size_t bytes_st = (pieces * 256 * 3 * sizeof(float) + 255) & ~static_cast<size_t>(255);
       const size_t bytes_cnt = static_cast<size_t>(R) * sizeof(unsigned);
-      // a failed scratch allocation only means no split (its error is cleared)
-      if (cudaMallocFromPoolAsync(&scratch, bytes_o + bytes_st + bytes_cnt, ds.pool, stream) !=
-          cudaSuccess) {
+      const size_t need = bytes_o + bytes_st + bytes_cnt;
+      uint8_t *base = nullptr;
+      if (noalloc) {
+        if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH;
+        base = ds.noalloc;
+      } else if (cudaMallocFromPoolAsync(&scratch, need, ds.pool, stream) != cudaSuccess) {
+        // a failed scratch allocation only means no split (its error is cleared)
         scratch = nullptr;
         cudaGetLastError();
       } else {
-        uint8_t *base = static_cast<uint8_t *>(scratch);
+        base = static_cast<uint8_t *>(scratch);
+      }
+      if (base != nullptr) {
         if (cudaMemsetAsync(base + bytes_o + bytes_st, 0, bytes_cnt, stream) == cudaSuccess) {
           p.split_first = p.n_items - R;
           p.split_k = k;
@@ -204,7 +223,7 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
           p.part_cnt = reinterpret_cast<unsigned *>(base + bytes_o + bytes_st);
         } else {
           cudaGetLastError();
-          cudaFreeAsync(scratch, stream);
+          if (scratch != nullptr) cudaFreeAsync(scratch, stream);
           scratch = nullptr;
         }
       }
@@ -225,7 +244,7 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
 
 int fwd_common(bool bf16, const void *q, const void *k, const void *v, void *o, float *lse,
                int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
-               float thr, fa_stream_t stream) {
+               float thr, fa_stream_t stream, bool noalloc = false) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_HEADDIM;
@@ -254,7 +273,7 @@ int fwd_common(bool bf16, const void *q, const void *k, const void *v, void *o, 
   // d = 128 (3-5 % faster on every d = 128 workload, causal or not), one
   // warpgroup per Q tile for d = 64, where the split form was 2 % slower.
 #define FA_LAUNCH(DD, BB, SS, SLOT) \
-  launch<DD, BB, SS>(*ds, SLOT, q, k, v, o, lse, BH, N, causal, scale, thr, st)
+  launch<DD, BB, SS>(*ds, SLOT, q, k, v, o, lse, BH, N, causal, scale, thr, noalloc, st)
   if (d == 64) return bf16 ? FA_LAUNCH(64, true, false, 0) : FA_LAUNCH(64, false, false, 1);
   return bf16 ? FA_LAUNCH(128, true, true, 2) : FA_LAUNCH(128, false, true, 3);
 #undef FA_LAUNCH
@@ -282,6 +301,13 @@ int fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, 
               float rescale_threshold, fa_stream_t stream) {
   return fwd_common(fp16 == 0, q, k, v, o, lse, B, H, N, d, causal, scale, rescale_threshold,
                     stream);
+}
+
+int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                   int64_t H, int64_t N, int64_t d, int causal, float scale, int fp16,
+                   float rescale_threshold, fa_stream_t stream) {
+  return fwd_common(fp16 == 0, q, k, v, o, lse, B, H, N, d, causal, scale, rescale_threshold,
+                    stream, /*noalloc=*/true);
 }
 
 int fa_selftest_wait_timeout(int64_t timeout_us, int *gave_up, fa_stream_t stream) {
@@ -331,6 +357,8 @@ const char *fa_strerror(int code) {
     case FA_ERR_OPTION:
       return "option out of range (rescale_threshold in [0, FA_MAX_RESCALE_THRESHOLD], "
              "self-test limit in [1, 1e6] us)";
+    case FA_ERR_SCRATCH:
+      return "fa_fwd_noalloc: the split schedule needs more than FA_NOALLOC_SCRATCH_BYTES";
     default: return "unknown error code";
   }
 }

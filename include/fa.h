@@ -65,8 +65,12 @@ typedef void *fa_stream_t;
 #define FA_ERR_TIMEOUT (-9)        /* a pipeline wait inside the kernel gave up */
 #define FA_ERR_ALIAS (-10)         /* an output overlaps an input or the other output */
 #define FA_ERR_OPTION (-11)        /* an option (rescale threshold, self-test limit) out of range */
+#define FA_ERR_SCRATCH (-12)       /* fa_fwd_noalloc: the call needs more than its fixed scratch */
 
 #define FA_MAX_N (1 << 20)         /* longest sequence accepted */
+
+/* Bytes of the fixed device array that serves fa_fwd_noalloc's scratch. */
+#define FA_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 /* Rescale threshold used by fa_fwd and fa_fwd_fp16, in log2 units of the
  * scaled logits (see fa_fwd_ex). */
@@ -117,6 +121,31 @@ int fa_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *lse
 int fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
               int64_t H, int64_t N, int64_t d, int causal, float scale, int fp16,
               float rescale_threshold, fa_stream_t stream);
+
+/*
+ * fa_fwd_noalloc -- fa_fwd_ex that never allocates device memory.
+ *
+ * The pages have no counterpart to this entry point: it is a deployment
+ * variant of this library for callers that must not allocate device memory
+ * during a call.  The wave-tail split's scratch (see Ownership above) comes
+ * from one fixed array of FA_NOALLOC_SCRATCH_BYTES in the library's device
+ * memory, located once per device (cudaGetSymbolAddress) when the library
+ * first sets the device up, instead of from the memory pool.  A call whose
+ * split needs more than that -- 134,144 bytes per piece (d = 128) plus 4 per
+ * split item, so at most 125 pieces; e.g. the 144 pieces of a non-causal
+ * [8,16,4096,128] call on 152 SMs -- is rejected with FA_ERR_SCRATCH before
+ * anything is launched (o and lse are not written); fa_fwd_ex serves it.
+ * Calls that need no scratch (causal, d = 64, or a last round that is not
+ * split) are always accepted, and the rest give bitwise fa_fwd_ex's result.
+ *
+ * The array is shared by every fa_fwd_noalloc call on the device, so these
+ * calls must not run concurrently: issue them on one stream, or order them
+ * with events.  Arguments, layout, ownership of q/k/v/o/lse and the other
+ * errors are fa_fwd_ex's.
+ */
+int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                   int64_t H, int64_t N, int64_t d, int causal, float scale, int fp16,
+                   float rescale_threshold, fa_stream_t stream);
 
 /*
  * fa_get_status -- synchronises `stream`, then returns and clears the

@@ -103,6 +103,25 @@ def test_fa_fwd_ex_option_errors(lib):
     assert ex(8.0, d=32, fp16=1) == fa.FA_ERR_HEADDIM
 
 
+def test_fa_fwd_noalloc_argument_errors(lib):
+    """The no-alloc entry point checks its arguments like fa_fwd_ex, before
+    touching the device."""
+    def na(thr=8.0, **kw):
+        a = dict(q=Q, k=K, v=V, o=O, lse=L, B=1, H=1, N=128, d=128, causal=0, scale=0.125,
+                 fp16=0)
+        a.update(kw)
+        return lib.fa_fwd_noalloc(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"],
+                                  a["N"], a["d"], a["causal"], a["scale"], a["fp16"], thr, None)
+    assert na(q=None) == fa.FA_ERR_NULL
+    assert na(N=0) == fa.FA_ERR_SHAPE
+    assert na(d=96) == fa.FA_ERR_HEADDIM
+    assert na(scale=0.0) == fa.FA_ERR_SCALE
+    assert na(thr=-1.0) == fa.FA_ERR_OPTION
+    assert na(o=Q) == fa.FA_ERR_ALIAS
+    assert fa.FA_ERR_SCRATCH == -12 and fa.FA_NOALLOC_SCRATCH_BYTES == 16 << 20
+    assert "FA_NOALLOC_SCRATCH_BYTES" in lib.fa_strerror(fa.FA_ERR_SCRATCH).decode()
+
+
 def test_selftest_argument_errors(lib):
     assert lib.fa_selftest_wait_timeout(1000, None, None) == fa.FA_ERR_NULL
     assert lib.fa_selftest_wait_timeout(0, 0x10000000, None) == fa.FA_ERR_OPTION
