@@ -147,7 +147,7 @@ template <int D, bool BF16, bool SPLIT>
 int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *v, void *o,
            float *lse, int64_t BH, int64_t N, int causal, float scale, float thr, bool noalloc,
            cudaStream_t stream) {
-  using C = fa::Cfg<D, BF16>;
+  using C = fa::Cfg<D, BF16, SPLIT>;
   auto kernel = fa::fa_fwd_kernel<D, BF16, SPLIT>;
   std::call_once(ds.attr_once[slot], [&] {
     cudaError_t e =

@@ -9,17 +9,22 @@
 // tiles are shared and no warp reduces another's output).
 //
 // Roles inside the CTA (FlashAttention v4 Blackwell pipeline diagram, the
-// producer / MMA / softmax lanes and the pseudo-code panel):
-//   warps 0-7  softmax: online softmax, O rescale and epilogue (O / l,
-//              logsumexp).  Two organisations (template SPLIT):
-//              false: warps 0-3 own Q tile 0, warps 4-7 own Q tile 1;
-//              true:  all eight warps take both tiles' S in turn, warps w and
-//              w + 4 splitting the columns of the rows of lane quadrant w % 4
-//              (about half the softmax latency per tile; used for d = 128)
-//   warp  8    MMA issue (one thread) + tensor-memory allocation
-//   warp  9    TMA producer (one thread): Q tiles and a K/V ring
-//   warps 10-11 idle (they complete the third warpgroup, whose registers
-//              are handed to the softmax groups with setmaxnreg)
+// producer / MMA / softmax lanes and the pseudo-code panel), by template
+// SPLIT:
+//   SPLIT (d = 128), 640 threads:
+//     warps 0-15  softmax, two groups of eight: warps 0-7 own Q tile 0 and
+//                 warps 8-15 Q tile 1, so the two tiles' softmax runs
+//                 concurrently; in a group, warps w and w + 4 split the 128
+//                 columns of the rows of lane quadrant w % 4 (about half the
+//                 softmax latency of one warp per row); each group also runs
+//                 its tile's epilogue (O / l, logsumexp)
+//     warp  16    MMA issue (one elected lane) + tensor-memory allocation
+//     warp  17    TMA producer (one thread): Q tiles and a K/V ring
+//     warps 18-19 idle (they complete the fifth warpgroup, whose registers
+//                 go to the softmax warpgroups through setmaxnreg)
+//   !SPLIT (d = 64), 384 threads: warps 0-3 own Q tile 0 and 4-7 Q tile 1,
+//     one thread per row over all columns; warp 8 MMA, warp 9 TMA, warps
+//     10-11 idle
 //
 // Tensor memory (512 columns x 128 lanes, 32-bit cells):
 //   S0 [0,128)   S1 [128,256)   O0 [256,256+D)   O1 [256+D,256+2D)
@@ -76,7 +81,7 @@ struct Params {
   unsigned *part_cnt;   // [split item]: pieces finished (zero before the launch)
 };
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool SPLIT>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
   static constexpr int kRows = 128;                   // Q rows per tile, keys per block
@@ -93,17 +98,24 @@ struct Cfg {
   static constexpr int kDrain = kOFull + 2;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag, merge flag
-  static constexpr int kXchOff = (kMiscOff + 16 + 15) & ~15;  // softmax row exchange, 4 KB
-  static constexpr int kSmemBytes = kXchOff + 2 * 2 * 2 * 128 * 4 + 1024;  // + base alignment slack
+  // softmax row exchange: [tile][parity][half][value][row] floats, 8 KB
+  static constexpr int kXchOff = (kMiscOff + 16 + 15) & ~15;
+  static constexpr int kSmemBytes = kXchOff + 2 * 2 * 2 * 2 * 128 * 4 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   // tensor-memory column of S_t and O_t for Q tile t
   static __device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
   static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + D * t; }
   static constexpr uint32_t kIdescS = idesc_f16(BF16, false, 128, 128);
   static constexpr uint32_t kIdescO = idesc_f16(BF16, true, 128, D);
-  static constexpr int kThreads = 384;  // three warpgroups
-  // setmaxnreg split: 2 x 128 x 208 + 128 x 88 = 384 x 168 (the launch budget)
-  static constexpr uint32_t kRegsSoftmax = 208, kRegsOther = 88;
+  // Column split (d = 128): five warpgroups -- four of softmax (eight warps
+  // per Q tile) and one with the MMA and TMA warps -- launched at 96
+  // registers a thread (five warps share each SMSP's 16384), then
+  // setmaxnreg 4 x 128 x 104 + 128 x 56 <= 640 x 96.  Otherwise three
+  // warpgroups (384 threads): 2 x 128 x 208 + 128 x 88 = 384 x 168.
+  static constexpr int kThreads = SPLIT ? 640 : 384;
+  static constexpr int kSoftmaxWarps = SPLIT ? 16 : 8;
+  static constexpr int kMmaWarp = kSoftmaxWarps, kTmaWarp = kSoftmaxWarps + 1;
+  static constexpr uint32_t kRegsSoftmax = SPLIT ? 104 : 208, kRegsOther = SPLIT ? 56 : 88;
 };
 
 struct Item {
@@ -220,19 +232,21 @@ __device__ __forceinline__ uint64_t unpack2(uint32_t v) {
   }
 }
 
-// Stores a 128-byte segment of each of a warp's 32 rows (8 chunks of 16 B
-// per lane, lane = row) so that every store instruction writes whole 128-byte
-// segments: within each group of 8 lanes an 8x8 transpose of the 16-byte
-// chunks (three xor-shuffle stages) leaves lane i of the group holding chunk
-// i of the group's 8 rows.  Row r of the warp is at row0 + r * stride bytes;
-// rows r >= rows_valid are not written.
-__device__ __forceinline__ void store_rows_128B(uint4 (&v)[8], uint8_t *row0, size_t stride,
-                                                int rows_valid, uint32_t lane) {
+// Stores a segment of NC 16-byte chunks (NC = 8: 128 bytes, NC = 4: 64
+// bytes) of each of a warp's 32 rows (lane = row) so that every store
+// instruction writes whole segments: within each group of NC lanes an NC x NC
+// transpose of the chunks (log2(NC) xor-shuffle stages) leaves lane i of the
+// group holding chunk i of the group's NC rows.  Row r of the warp is at
+// row0 + r * stride bytes; rows r >= rows_valid are not written.
+template <int NC>
+__device__ __forceinline__ void store_rows(uint4 (&v)[NC], uint8_t *row0, size_t stride,
+                                           int rows_valid, uint32_t lane) {
+  static_assert(NC == 4 || NC == 8, "4 or 8 chunks per row");
 #pragma unroll
-  for (int k = 4; k >= 1; k >>= 1) {
+  for (int k = NC / 2; k >= 1; k >>= 1) {
     const bool hi = (lane & k) != 0;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < NC; ++c) {
       if (c & k) continue;
       const uint4 send = hi ? v[c] : v[c | k];
       uint4 recv;
@@ -244,20 +258,20 @@ __device__ __forceinline__ void store_rows_128B(uint4 (&v)[8], uint8_t *row0, si
       else v[c | k] = recv;
     }
   }
-  const int g = static_cast<int>(lane >> 3), i = static_cast<int>(lane & 7);
+  const int g = static_cast<int>(lane) / NC, i = static_cast<int>(lane) % NC;
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    const int row = 8 * g + r;
+  for (int r = 0; r < NC; ++r) {
+    const int row = NC * g + r;
     if (row < rows_valid)
       *reinterpret_cast<uint4 *>(row0 + static_cast<size_t>(row) * stride + 16 * i) = v[r];
   }
 }
 
 template <int D, bool BF16, bool SPLIT>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(Cfg<D, BF16, SPLIT>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
-  using C = Cfg<D, BF16>;
+  using C = Cfg<D, BF16, SPLIT>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte-swizzled tiles.
   const uint32_t raw = smem_u32(smem_raw);
@@ -290,12 +304,12 @@ __global__ void __launch_bounds__(384, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 9 && lane == 0) {
+  if (warp == C::kTmaWarp && lane == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
   }
-  if (warp == 8) {
+  if (warp == C::kMmaWarp) {
     tmem_alloc(smem_u32(tmem_base_slot), C::kTmemCols);
     tmem_relinquish();
   }
@@ -304,11 +318,11 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_base_slot;
 
-  if (warp >= 8) {
+  if (warp >= C::kSoftmaxWarps) {
     // Each role's code sits under its own setmaxnreg, so the compiler sizes
     // it for that role's register budget only.
     regs_dec<C::kRegsOther>();
-    if (warp == 9) {
+    if (warp == C::kTmaWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol_q = l2_policy_evict_first();
@@ -362,7 +376,7 @@ __global__ void __launch_bounds__(384, 1)
       for (int t = 0; t < 2; ++t)
         if (q_loads[t]) wait_drain(bar(C::kQFull + t), (q_loads[t] - 1) & 1u);
     }
-    } else if (warp == 8) {
+    } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------- MMA issue
     // The whole warp runs this loop (waits included) and one elected lane
     // issues the MMAs and commits: a converged warp issues faster than a
@@ -661,30 +675,35 @@ __global__ void __launch_bounds__(384, 1)
             v8[c * 4 + u] = make_uint4(pk16[4 * u], pk16[4 * u + 1], pk16[4 * u + 2],
                                        pk16[4 * u + 3]);
         }
-        store_rows_128B(v8, orow0 + 128 * half, static_cast<size_t>(D) * 2, rows_valid, lane);
+        store_rows<8>(v8, orow0 + 128 * half, static_cast<size_t>(D) * 2, rows_valid, lane);
       }
       if (live) p.lse[row_off] = (m + lg2_approx(l)) * 0.6931471805599453f;
     }
     tc_fence_before();
     } else {
     // ------------------------------------------ softmax, column split
-    // All eight softmax warps work on whichever tile's S is ready (S0(j),
-    // S1(j), S0(j+1), ... in the order the MMAs produce them).  Warp w takes
-    // the 32 rows of tensor-memory lane quadrant q = w % 4 (one thread per
-    // row) and the 64 columns [64h, 64h + 64) of S, h = w / 4, so two warps
-    // share each SMSP's rows and the softmax of one tile takes about half
-    // as long.  The two warps of a quadrant exchange partial row maxima
-    // (and, at the end, partial row sums) through shared memory.
-    const int q = warp & 3, hf = warp >> 2;
+    // Two groups of eight warps, one per Q tile (warps 0-7: tile 0, 8-15:
+    // tile 1), so the two tiles' softmax runs concurrently.  In a group,
+    // warp w takes the 32 rows of tensor-memory lane quadrant q = w % 4 (one
+    // thread per row) and the 64 columns [64h, 64h + 64) of S,
+    // h = (w / 4) % 2: two warps share a quadrant's rows, so the softmax of a
+    // block takes about half as long as with one warp per row.  The two
+    // warps of a quadrant exchange partial row maxima (and, at the end,
+    // partial row sums) through shared memory.
+    const int t = warp >> 3;  // this group's Q tile
+    const int q = warp & 3, hf = (warp >> 2) & 1;
     const uint32_t lane_base = q * 32u;
     const int row = static_cast<int>(lane_base + lane);
     const uint32_t t_lane = tmem + (lane_base << 16);
-    float *xch = reinterpret_cast<float *>(smem + C::kXchOff);  // [parity][half][value][row]
-    auto xslot = [&](uint32_t par, int h, int val) { return xch + ((par * 2 + h) * 2 + val) * 128 + row; };
-    const uint32_t pair_bar = 1u + static_cast<uint32_t>(q);  // named barrier of the quadrant's two warps
+    float *xch = reinterpret_cast<float *>(smem + C::kXchOff);  // [tile][parity][half][value][row]
+    auto xslot = [&](uint32_t par, int h, int val) {
+      return xch + (((t * 2 + par) * 2 + h) * 2 + val) * 128 + row;
+    };
+    // named barrier of the quadrant's two warps in this group (1..8)
+    const uint32_t pair_bar = 1u + static_cast<uint32_t>(q) + 4u * static_cast<uint32_t>(t);
     auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
-    // all eight softmax warps (named barrier 5)
-    auto softmax_sync = [&]() { asm volatile("bar.sync 5, 256;" ::: "memory"); };
+    // all sixteen softmax warps (named barrier 9)
+    auto softmax_sync = [&]() { asm volatile("bar.sync 9, 512;" ::: "memory"); };
     volatile unsigned *merge_flag = reinterpret_cast<volatile unsigned *>(smem + C::kMiscOff + 8);
     // Merge of the pieces of a split item, tile t, this thread's row and
     // half of the columns: with M the largest of the pieces' maxima, piece
@@ -718,42 +737,46 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       const float inv = 1.f / wr;
-      float acc[D / 2];
-#pragma unroll
-      for (int e = 0; e < D / 2; ++e) acc[e] = 0.f;
-#pragma unroll
-      for (int c = 0; c < kMaxSplit; ++c) {
-        if (c < k) {
-          const float wc = w[c] * inv;
-          const float4 *src =
-              p.part_o + (static_cast<size_t>(first + c) * (D / 4) + (D / 8) * hf) * 256 + prow_in_item;
-#pragma unroll
-          for (int u = 0; u < D / 8; ++u) {
-            const float4 x = __ldcg(src + u * 256);
-            acc[4 * u] = fmaf(wc, x.x, acc[4 * u]);
-            acc[4 * u + 1] = fmaf(wc, x.y, acc[4 * u + 1]);
-            acc[4 * u + 2] = fmaf(wc, x.z, acc[4 * u + 2]);
-            acc[4 * u + 3] = fmaf(wc, x.w, acc[4 * u + 3]);
-          }
-        }
-      }
-      uint4 v8[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        v8[u] = make_uint4(pack2<BF16>(acc[8 * u], acc[8 * u + 1]),
-                           pack2<BF16>(acc[8 * u + 2], acc[8 * u + 3]),
-                           pack2<BF16>(acc[8 * u + 4], acc[8 * u + 5]),
-                           pack2<BF16>(acc[8 * u + 6], acc[8 * u + 7]));
       const int q_idx = (it.qt0 + t) * 128 + row;
       const size_t row_off = static_cast<size_t>(it.bh) * p.N + q_idx;
-      store_rows_128B(v8,
-                      reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.o) +
-                                                  (row_off - lane) * D + (D / 2) * hf),
-                      static_cast<size_t>(D) * 2, p.N - (q_idx - static_cast<int>(lane)), lane);
+      uint8_t *orow0 = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.o) +
+                                                   (row_off - lane) * D + (D / 2) * hf);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {  // 32 columns at a time
+        float acc[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int c = 0; c < kMaxSplit; ++c) {
+          if (c < k) {
+            const float wc = w[c] * inv;
+            const float4 *src = p.part_o +
+                                (static_cast<size_t>(first + c) * (D / 4) + (D / 8) * hf + 8 * hh) * 256 +
+                                prow_in_item;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const float4 x = __ldcg(src + u * 256);
+              acc[4 * u] = fmaf(wc, x.x, acc[4 * u]);
+              acc[4 * u + 1] = fmaf(wc, x.y, acc[4 * u + 1]);
+              acc[4 * u + 2] = fmaf(wc, x.z, acc[4 * u + 2]);
+              acc[4 * u + 3] = fmaf(wc, x.w, acc[4 * u + 3]);
+            }
+          }
+        }
+        uint4 v4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          v4[u] = make_uint4(pack2<BF16>(acc[8 * u], acc[8 * u + 1]),
+                             pack2<BF16>(acc[8 * u + 2], acc[8 * u + 3]),
+                             pack2<BF16>(acc[8 * u + 4], acc[8 * u + 5]),
+                             pack2<BF16>(acc[8 * u + 6], acc[8 * u + 7]));
+        store_rows<4>(v4, orow0 + 64 * hh, static_cast<size_t>(D) * 2,
+                      p.N - (q_idx - static_cast<int>(lane)), lane);
+      }
       if (q_idx < p.N && hf == 0) p.lse[row_off] = (M + lg2_approx(wl)) * 0.6931471805599453f;
     };
     const float sl2 = p.scale_log2;
-    uint32_t s_par = 0, o_par = 0, xpar = 0;  // barrier phase bits per tile, exchange parity
+    uint32_t s_par = 0, o_par = 0, xpar = 0;  // barrier phase bits, exchange parity
     // bar.sync cannot time out, so a warp whose wait gave up (ok == false)
     // keeps walking the same sequence of blocks, doing no work but taking
     // part in every pair barrier, so its partner can never be left waiting.
@@ -762,26 +785,26 @@ __global__ void __launch_bounds__(384, 1)
       const int item = round_item(round, p);
       if (item < 0) continue;
       const Item it = decode_unit(item, p);
-      const int n_max = it.n0 > it.n1 ? it.n0 : it.n1;
-      // per tile: running max (log2 units), this half's sums of P and of P
-      // corrected for the rounding of each block's largest value
-      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, r0 = 0.f, r1 = 0.f;
-      // epilogue of tile t: O / l to memory, logsumexp (one pair barrier on
-      // every path, like a block)
-      auto epilogue = [&](int t) {
-        if (ok) ok = wait_bar(bar(C::kOFull + t), (o_par >> t) & 1u, abort_flag, p.status);
+      const int n = t ? it.n1 : it.n0;  // this tile's K/V blocks (0: no tile 1)
+      // running max (log2 units), this half's sums of P and of P corrected
+      // for the rounding of each block's largest value
+      float m = -INFINITY, l = 0.f, r = 0.f;
+      // epilogue: O / l to memory, logsumexp (one pair barrier on every
+      // path, like a block)
+      auto epilogue = [&]() {
+        if (ok) ok = wait_bar(bar(C::kOFull + t), o_par, abort_flag, p.status);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
           pair_sync();
           return;
         }
-        o_par ^= 1u << t;
+        o_par ^= 1u;
         tc_fence_after();
-        *xslot(xpar, hf, 0) = t ? l1 : l0;
-        *xslot(xpar, hf, 1) = t ? r1 : r0;
+        *xslot(xpar, hf, 0) = l;
+        *xslot(xpar, hf, 1) = r;
         pair_sync();
-        const float lsum = (t ? l1 : l0) + *xslot(xpar, hf ^ 1, 0);
-        const float rsum = (t ? r1 : r0) + *xslot(xpar, hf ^ 1, 1);
+        const float lsum = l + *xslot(xpar, hf ^ 1, 0);
+        const float rsum = r + *xslot(xpar, hf ^ 1, 1);
         xpar ^= 1u;
         const float inv_l = 1.f / rsum;
         const uint64_t inv_l2 = f2(inv_l, inv_l);
@@ -811,52 +834,52 @@ __global__ void __launch_bounds__(384, 1)
           }
           if (hf == 0) {
             float *st = p.part_st + static_cast<size_t>(it.piece) * 3 * 256 + prow;
-            st[0] = t ? m1 : m0;
+            st[0] = m;
             st[256] = lsum;
             st[512] = rsum;
           }
           return;
         }
-        uint4 v8[8];
+        // this warp's first row, its half of the columns; rows D * 2 bytes
+        // apart; 32 columns (64 bytes of each row) at a time
+        uint8_t *orow0 = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.o) +
+                                                     (row_off - lane) * D + (D / 2) * hf);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t orr[32];
           tmem_ld32(tO + 32 * c, orr);
           tmem_ld_wait(orr);
-          uint32_t pk16[16];
+          uint4 v4[4];
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            float a, b;
-            f2_split(fmul2(f2(__uint_as_float(orr[2 * u]), __uint_as_float(orr[2 * u + 1])),
-                           inv_l2),
-                     a, b);
-            pk16[u] = pack2<BF16>(a, b);
+          for (int u = 0; u < 4; ++u) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float a, b;
+              f2_split(fmul2(f2(__uint_as_float(orr[8 * u + 2 * e]),
+                                __uint_as_float(orr[8 * u + 2 * e + 1])),
+                             inv_l2),
+                       a, b);
+              w4[e] = pack2<BF16>(a, b);
+            }
+            v4[u] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            v8[c * 4 + u] = make_uint4(pk16[4 * u], pk16[4 * u + 1], pk16[4 * u + 2],
-                                       pk16[4 * u + 3]);
+          store_rows<4>(v4, orow0 + 64 * c, static_cast<size_t>(D) * 2,
+                        p.N - (q_idx - static_cast<int>(lane)), lane);
         }
-        // this warp's first row, its half of the columns; rows D * 2 bytes apart
-        store_rows_128B(v8,
-                        reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.o) +
-                                                    (row_off - lane) * D + (D / 2) * hf),
-                        static_cast<size_t>(D) * 2, p.N - (q_idx - static_cast<int>(lane)),
-                        lane);
         if (live && hf == 0)
-          p.lse[row_off] = ((t ? m1 : m0) + lg2_approx(lsum)) * 0.6931471805599453f;
+          p.lse[row_off] = (m + lg2_approx(lsum)) * 0.6931471805599453f;
       };
-      for (int j = 0; j < n_max; ++j) {
-        for (int t = 0; t < 2; ++t) {
-          if (j >= (t ? it.n1 : it.n0)) continue;
+      for (int j = 0; j < n; ++j) {
+        {
           const int qt = it.qt0 + t;
-          if (ok) ok = wait_bar(bar(C::kSFull + t), (s_par >> t) & 1u, abort_flag, p.status);
+          if (ok) ok = wait_bar(bar(C::kSFull + t), s_par, abort_flag, p.status);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) {  // failed: keep the pair barrier count in step, do nothing else
             pair_sync();
             continue;
           }
-          s_par ^= 1u << t;
+          s_par ^= 1u;
           tc_fence_after();
           const uint32_t tS = t_lane + C::col_s(t);
           uint32_t sr[2][32];
@@ -895,7 +918,6 @@ __global__ void __launch_bounds__(384, 1)
           pair_sync();
           const float rmax = fmaxf(hmax, *xslot(xpar, hf ^ 1, 0));
           xpar ^= 1u;
-          float m = t ? m1 : m0;
           const float m_cand = fmaxf(m, rmax * sl2);
           const bool need = (m_cand - m) > p.rescale_thr;
           float alpha = 1.f;
@@ -910,16 +932,19 @@ __global__ void __launch_bounds__(384, 1)
           const uint64_t sl2_2 = f2(sl2, sl2);
           const uint64_t negm_2 = f2(-m, -m);
           uint64_t sx2[2] = {0, 0};
-          uint32_t pk[32];
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            float x0, x1;
-            f2_split(ffma2(f2(s[c], s[c + 1]), sl2_2, negm_2), x0, x1);
-            const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-            pk[c >> 1] = pack2<BF16>(e0, e1);
-            sx2[(c >> 1) & 1] = fadd2(sx2[(c >> 1) & 1], f2(e0, e1));
+          for (int hh = 0; hh < 2; ++hh) {  // two stores of 16 columns: fewer live registers
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 32 * hh; c < 32 * hh + 32; c += 2) {
+              float x0, x1;
+              f2_split(ffma2(f2(s[c], s[c + 1]), sl2_2, negm_2), x0, x1);
+              const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+              pk[(c >> 1) & 15] = pack2<BF16>(e0, e1);
+              sx2[(c >> 1) & 1] = fadd2(sx2[(c >> 1) & 1], f2(e0, e1));
+            }
+            tmem_st16(tS + 32 * hf + 16 * hh, pk);
           }
-          tmem_st32(tS + 32 * hf, pk);
           float sum_x, sum_r;
           {
             float a, b;
@@ -935,39 +960,29 @@ __global__ void __launch_bounds__(384, 1)
               sum_r += __bfloat162float(__float2bfloat16_rn(top)) - top;
             }
           }
-          if (t) {
-            m1 = m;
-            l1 = l1 * alpha + sum_x;
-            r1 = r1 * alpha + sum_r;
-          } else {
-            m0 = m;
-            l0 = l0 * alpha + sum_x;
-            r0 = r0 * alpha + sum_r;
-          }
+          l = l * alpha + sum_x;
+          r = r * alpha + sum_r;
           // Conditional rescale of this half of the running output (v4
           // pseudo-code panel: "if need_rescale(m, m_new): acc *= exp(m -
           // m_new)").  PV_t(j-1) is complete: its commit precedes S_t(j)'s;
           // PV_t(j) waits for this block's signal.
           if (j > 0 && __any_sync(0xffffffffu, need)) {
             const uint32_t tO = t_lane + C::col_o(t) + (D / 2) * hf;
-            uint32_t orr[D / 64][32];
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) tmem_ld32(tO + 32 * c, orr[c]);
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) tmem_ld_wait(orr[c]);
             const uint64_t alpha2 = f2(alpha, alpha);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
+            for (int c = 0; c < D / 64; ++c) {  // 32 columns at a time
+              uint32_t orr[32];
+              tmem_ld32(tO + 32 * c, orr);
+              tmem_ld_wait(orr);
 #pragma unroll
               for (int u = 0; u < 32; u += 2) {
                 float a, b;
-                f2_split(fmul2(f2(__uint_as_float(orr[c][u]), __uint_as_float(orr[c][u + 1])),
-                               alpha2),
+                f2_split(fmul2(f2(__uint_as_float(orr[u]), __uint_as_float(orr[u + 1])), alpha2),
                          a, b);
-                orr[c][u] = __float_as_uint(a);
-                orr[c][u + 1] = __float_as_uint(b);
+                orr[u] = __float_as_uint(a);
+                orr[u + 1] = __float_as_uint(b);
               }
-              tmem_st32(tO + 32 * c, orr[c]);
+              tmem_st32(tO + 32 * c, orr);
             }
           }
           tmem_st_wait();
@@ -975,12 +990,8 @@ __global__ void __launch_bounds__(384, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(C::kPFull + t));
         }
-        // tile 0 is done after block n0 - 1: its epilogue runs while the
-        // tensor core works on tile 1's next block
-        if (it.n1 > 0 && j == it.n0 - 1) epilogue(0);
       }
-      if (it.n1 == 0) epilogue(0);
-      else epilogue(1);
+      if (n > 0) epilogue();
       if (it.piece >= 0) {
         // The piece's results are in scratch memory: make them visible to
         // the whole device, count the piece, and if it was the item's last
@@ -996,9 +1007,7 @@ __global__ void __launch_bounds__(384, 1)
           *merge_flag = last;
         }
         softmax_sync();
-        if (ok && *merge_flag) {
-          for (int t = 0; t < (it.n1 > 0 ? 2 : 1); ++t) merge(it, t);
-        }
+        if (ok && *merge_flag && n > 0) merge(it, t);
       }
     }
     tc_fence_before();
@@ -1006,7 +1015,7 @@ __global__ void __launch_bounds__(384, 1)
   }
 
   __syncthreads();
-  if (warp == 8) {
+  if (warp == C::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
