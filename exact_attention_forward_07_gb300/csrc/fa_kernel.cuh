@@ -742,7 +742,7 @@ __global__ void __launch_bounds__(Cfg<D, BF16, SPLIT>::kThreads, 1)
       uint8_t *orow0 = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.o) +
                                                    (row_off - lane) * D + (D / 2) * hf);
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {  // 32 columns at a time
+      for (int hh = 0; hh < D / 64; ++hh) {  // 32 columns at a time
         float acc[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) acc[e] = 0.f;
@@ -812,7 +812,6 @@ __global__ void __launch_bounds__(Cfg<D, BF16, SPLIT>::kThreads, 1)
         const bool live = q_idx < p.N;
         const size_t row_off = (static_cast<size_t>(it.bh) * p.N + q_idx);
         const uint32_t tO = t_lane + C::col_o(t) + (D / 2) * hf;
-        static_assert(!SPLIT || D == 128, "column split stores 64 columns (128 bytes) per warp");
         if (it.piece >= 0) {
           // a piece of a split item: its O normalised by its own sum (fp32)
           // and its row statistics go to scratch memory for the merge, in a
@@ -821,7 +820,7 @@ __global__ void __launch_bounds__(Cfg<D, BF16, SPLIT>::kThreads, 1)
           const int prow = t * 128 + row;
           float4 *dst = p.part_o + (static_cast<size_t>(it.piece) * (D / 4) + (D / 8) * hf) * 256 + prow;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < D / 64; ++c) {
             uint32_t orr[32];
             tmem_ld32(tO + 32 * c, orr);
             tmem_ld_wait(orr);
@@ -845,7 +844,7 @@ __global__ void __launch_bounds__(Cfg<D, BF16, SPLIT>::kThreads, 1)
         uint8_t *orow0 = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.o) +
                                                      (row_off - lane) * D + (D / 2) * hf);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t orr[32];
           tmem_ld32(tO + 32 * c, orr);
           tmem_ld_wait(orr);
