@@ -143,12 +143,12 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
-template <int D, bool BF16, bool SPLIT>
+template <int D, bool BF16>
 int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *v, void *o,
            float *lse, int64_t BH, int64_t N, int causal, float scale, float thr, bool noalloc,
            cudaStream_t stream) {
-  using C = fa::Cfg<D, BF16, SPLIT>;
-  auto kernel = fa::fa_fwd_kernel<D, BF16, SPLIT>;
+  using C = fa::Cfg<D, BF16>;
+  auto kernel = fa::fa_fwd_kernel<D, BF16>;
   std::call_once(ds.attr_once[slot], [&] {
     cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -190,7 +190,7 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
   p.part_st = nullptr;
   p.part_cnt = nullptr;
   void *scratch = nullptr;  // pool memory to give back after the launch
-  if (SPLIT && !causal && (noalloc || ds.pool != nullptr)) {
+  if (!causal && (noalloc || ds.pool != nullptr)) {
     const int G = ds.sm_count;
     const int R = p.n_items % G;
     int k = R > 0 ? G / R : 0;
@@ -269,13 +269,10 @@ int fwd_common(bool bf16, const void *q, const void *k, const void *v, void *o, 
   int rc = device_state(&ds);
   if (rc != FA_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // Softmax organisation (measured on GB300): the column-split form for
-  // d = 128 (3-5 % faster on every d = 128 workload, causal or not), one
-  // warpgroup per Q tile for d = 64, where the split form was 2 % slower.
-#define FA_LAUNCH(DD, BB, SS, SLOT) \
-  launch<DD, BB, SS>(*ds, SLOT, q, k, v, o, lse, BH, N, causal, scale, thr, noalloc, st)
-  if (d == 64) return bf16 ? FA_LAUNCH(64, true, false, 0) : FA_LAUNCH(64, false, false, 1);
-  return bf16 ? FA_LAUNCH(128, true, true, 2) : FA_LAUNCH(128, false, true, 3);
+#define FA_LAUNCH(DD, BB, SLOT) \
+  launch<DD, BB>(*ds, SLOT, q, k, v, o, lse, BH, N, causal, scale, thr, noalloc, st)
+  if (d == 64) return bf16 ? FA_LAUNCH(64, true, 0) : FA_LAUNCH(64, false, 1);
+  return bf16 ? FA_LAUNCH(128, true, 2) : FA_LAUNCH(128, false, 3);
 #undef FA_LAUNCH
 }
 

@@ -9,22 +9,17 @@
 // tiles are shared and no warp reduces another's output).
 //
 // Roles inside the CTA (FlashAttention v4 Blackwell pipeline diagram, the
-// producer / MMA / softmax lanes and the pseudo-code panel), by template
-// SPLIT:
-//   SPLIT (d = 128), 640 threads:
-//     warps 0-15  softmax, two groups of eight: warps 0-7 own Q tile 0 and
-//                 warps 8-15 Q tile 1, so the two tiles' softmax runs
-//                 concurrently; in a group, warps w and w + 4 split the 128
-//                 columns of the rows of lane quadrant w % 4 (about half the
-//                 softmax latency of one warp per row); each group also runs
-//                 its tile's epilogue (O / l, logsumexp)
-//     warp  16    MMA issue (one elected lane) + tensor-memory allocation
-//     warp  17    TMA producer (one thread): Q tiles and a K/V ring
-//     warps 18-19 idle (they complete the fifth warpgroup, whose registers
-//                 go to the softmax warpgroups through setmaxnreg)
-//   !SPLIT (d = 64), 384 threads: warps 0-3 own Q tile 0 and 4-7 Q tile 1,
-//     one thread per row over all columns; warp 8 MMA, warp 9 TMA, warps
-//     10-11 idle
+// producer / MMA / softmax lanes and the pseudo-code panel), 640 threads:
+//   warps 0-15  softmax, two groups of eight: warps 0-7 own Q tile 0 and
+//               warps 8-15 Q tile 1, so the two tiles' softmax runs
+//               concurrently; in a group, warps w and w + 4 split the 128
+//               columns of S of the rows of lane quadrant w % 4 (about half
+//               the softmax latency of one warp per row); each group also
+//               runs its tile's epilogue (O / l, logsumexp)
+//   warp  16    MMA issue (one elected lane) + tensor-memory allocation
+//   warp  17    TMA producer (one thread): Q tiles and a K/V ring
+//   warps 18-19 idle (they complete the fifth warpgroup, whose registers
+//               go to the softmax warpgroups through setmaxnreg)
 //
 // Tensor memory (512 columns x 128 lanes, 32-bit cells):
 //   S0 [0,128)   S1 [128,256)   O0 [256,256+D)   O1 [256+D,256+2D)
@@ -81,7 +76,7 @@ struct Params {
   unsigned *part_cnt;   // [split item]: pieces finished (zero before the launch)
 };
 
-template <int D, bool BF16, bool SPLIT>
+template <int D, bool BF16>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
   static constexpr int kRows = 128;                   // Q rows per tile, keys per block
@@ -107,15 +102,14 @@ struct Cfg {
   static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + D * t; }
   static constexpr uint32_t kIdescS = idesc_f16(BF16, false, 128, 128);
   static constexpr uint32_t kIdescO = idesc_f16(BF16, true, 128, D);
-  // Column split (d = 128): five warpgroups -- four of softmax (eight warps
-  // per Q tile) and one with the MMA and TMA warps -- launched at 96
-  // registers a thread (five warps share each SMSP's 16384), then
-  // setmaxnreg 4 x 128 x 104 + 128 x 56 <= 640 x 96.  Otherwise three
-  // warpgroups (384 threads): 2 x 128 x 208 + 128 x 88 = 384 x 168.
-  static constexpr int kThreads = SPLIT ? 640 : 384;
-  static constexpr int kSoftmaxWarps = SPLIT ? 16 : 8;
+  // Five warpgroups -- four of softmax (eight warps per Q tile) and one with
+  // the MMA and TMA warps -- launched at 96 registers a thread (five warps
+  // share each SMSP's 16384), then setmaxnreg 4 x 128 x 104 + 128 x 56
+  // <= 640 x 96.
+  static constexpr int kThreads = 640;
+  static constexpr int kSoftmaxWarps = 16;
   static constexpr int kMmaWarp = kSoftmaxWarps, kTmaWarp = kSoftmaxWarps + 1;
-  static constexpr uint32_t kRegsSoftmax = SPLIT ? 104 : 208, kRegsOther = SPLIT ? 56 : 88;
+  static constexpr uint32_t kRegsSoftmax = 104, kRegsOther = 56;
 };
 
 struct Item {
@@ -221,17 +215,6 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
-// The two 16-bit values of a packed pair, widened back to fp32 (exact).
-template <bool BF16>
-__device__ __forceinline__ uint64_t unpack2(uint32_t v) {
-  if constexpr (BF16) {
-    return f2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
-  } else {
-    __half2 h = *reinterpret_cast<__half2 *>(&v);
-    return f2(__low2float(h), __high2float(h));
-  }
-}
-
 // Stores a segment of NC 16-byte chunks (NC = 8: 128 bytes, NC = 4: 64
 // bytes) of each of a warp's 32 rows (lane = row) so that every store
 // instruction writes whole segments: within each group of NC lanes an NC x NC
@@ -267,11 +250,11 @@ __device__ __forceinline__ void store_rows(uint4 (&v)[NC], uint8_t *row0, size_t
   }
 }
 
-template <int D, bool BF16, bool SPLIT>
-__global__ void __launch_bounds__(Cfg<D, BF16, SPLIT>::kThreads, 1)
+template <int D, bool BF16>
+__global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
-  using C = Cfg<D, BF16, SPLIT>;
+  using C = Cfg<D, BF16>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte-swizzled tiles.
   const uint32_t raw = smem_u32(smem_raw);
@@ -297,7 +280,7 @@ __global__ void __launch_bounds__(Cfg<D, BF16, SPLIT>::kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::kSFull + t), 1);
-      mbar_init(bar(C::kPFull + t), SPLIT ? 8 : 4);  // one arrive per softmax warp
+      mbar_init(bar(C::kPFull + t), 8);  // one arrive per softmax warp of the tile's group
       mbar_init(bar(C::kOFull + t), 1);
     }
     mbar_init(bar(C::kDrain), 1);
@@ -509,178 +492,6 @@ __global__ void __launch_bounds__(Cfg<D, BF16, SPLIT>::kThreads, 1)
     }
   } else {
     regs_inc<C::kRegsSoftmax>();
-    if constexpr (!SPLIT) {
-    // ------------------------------------------ softmax, one group per tile
-    // Warps 0-3 handle Q tile 0 and warps 4-7 Q tile 1, one thread per row,
-    // all 128 columns; the two groups run their tiles concurrently.
-    const int t = warp >> 2;                      // Q tile of this group
-    const uint32_t lane_base = (warp & 3) * 32u;  // this warp's TMEM lane quadrant
-    const int row = static_cast<int>(lane_base + lane);
-    const uint32_t t_lane = tmem + (lane_base << 16);
-    const uint32_t tS = t_lane + C::col_s(t);
-    const uint32_t tO = t_lane + C::col_o(t);
-    const float sl2 = p.scale_log2;
-    uint32_t s_phase = 0, o_phase = 0;
-    bool ok = true;
-    for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_units; ++round) {
-      const int item = round_item(round, p);
-      if (item < 0) continue;
-      const Item it = decode_unit(item, p);
-      const int n = t ? it.n1 : it.n0;
-      if (n == 0) continue;
-      const int qt = it.qt0 + t;
-      const int q_idx = qt * 128 + row;
-      float m = -INFINITY, l = 0.f, lr = 0.f;  // max (log2 units), sums of P, of rounded P
-      for (int j = 0; j < n; ++j) {
-        ok = wait_bar(bar(C::kSFull + t), s_phase, abort_flag, p.status);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        s_phase ^= 1u;
-        tc_fence_after();
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sr[c]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
-        float s[128];
-#pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
-        // mask only where needed: the diagonal block (causal) or the ragged
-        // last block (non-causal, N % 128 != 0)
-        if (p.causal && j == qt) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c > row) s[c] = -INFINITY;
-        } else if (!p.causal && it.j0 + j == p.n_qtiles - 1 && (p.N & 127)) {
-          const int lim = p.N - (it.j0 + j) * 128;
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c >= lim) s[c] = -INFINITY;
-        }
-        // row max: three-input max over s[4..127] in four chains
-        float mx[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-        for (int c = 4; c < 124; c += 8) {
-          mx[0] = fmax3(mx[0], s[c], s[c + 1]);
-          mx[1] = fmax3(mx[1], s[c + 2], s[c + 3]);
-          mx[2] = fmax3(mx[2], s[c + 4], s[c + 5]);
-          mx[3] = fmax3(mx[3], s[c + 6], s[c + 7]);
-        }
-        mx[0] = fmax3(mx[0], s[124], s[125]);
-        mx[1] = fmax3(mx[1], s[126], s[127]);
-        const float rmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
-        const float m_cand = fmaxf(m, rmax * sl2);
-        const bool need = (m_cand - m) > p.rescale_thr;
-        float alpha = 1.f;
-        if (need) {
-          alpha = ex2_approx(m - m_cand);
-          m = m_cand;
-        }
-        // P = 2^(S*scale*log2e - m), rounded to the MMA's 16-bit type.  The
-        // logsumexp uses the fp32 row sum.  O is normalised by that sum plus,
-        // for bf16, the rounding error of the block's largest P: in a peaked
-        // row the dominant weight's rounding would otherwise show in O
-        // undivided, while the other elements' rounding errors average out.
-        const uint64_t sl2_2 = f2(sl2, sl2);
-        const uint64_t negm_2 = f2(-m, -m);
-        uint64_t sx2[2] = {0, 0};
-        uint32_t pk[2][32];
-#pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-          float x0, x1;
-          f2_split(ffma2(f2(s[c], s[c + 1]), sl2_2, negm_2), x0, x1);
-          const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-          pk[c >> 6][(c >> 1) & 31] = pack2<BF16>(e0, e1);
-          sx2[(c >> 1) & 1] = fadd2(sx2[(c >> 1) & 1], f2(e0, e1));
-        }
-        float sum_x, sum_r;
-        {
-          float a, b;
-          f2_split(fadd2(sx2[0], sx2[1]), a, b);
-          sum_x = a + b;
-          sum_r = sum_x;
-          if constexpr (BF16) {
-            const float top = ex2_approx(fmaf(rmax, sl2, -m));  // the block's largest P
-            sum_r += __bfloat162float(__float2bfloat16_rn(top)) - top;
-          }
-        }
-        tmem_st32(tS + 0, pk[0]);
-        tmem_st32(tS + 32, pk[1]);
-        l = l * alpha + sum_x;
-        lr = lr * alpha + sum_r;
-        // Conditional rescale of the running output (v4 pseudo-code panel:
-        // "if need_rescale(m, m_new): acc *= exp(m - m_new)"), done once the
-        // S values are no longer live.  PV(j-1) is complete: its commit
-        // precedes this block's S commit; PV(j) waits for this group's signal.
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
-          uint32_t orr[D / 32][32];
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + 32 * c, orr[c]);
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) tmem_ld_wait(orr[c]);
-          const uint64_t alpha2 = f2(alpha, alpha);
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-#pragma unroll
-            for (int u = 0; u < 32; u += 2) {
-              float a, b;
-              f2_split(fmul2(f2(__uint_as_float(orr[c][u]), __uint_as_float(orr[c][u + 1])),
-                             alpha2),
-                       a, b);
-              orr[c][u] = __float_as_uint(a);
-              orr[c][u + 1] = __float_as_uint(b);
-            }
-            tmem_st32(tO + 32 * c, orr[c]);
-          }
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::kPFull + t));
-      }
-      if (!ok) break;
-      // ------------------------------------------------------ epilogue
-      ok = wait_bar(bar(C::kOFull + t), o_phase, abort_flag, p.status);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      o_phase ^= 1u;
-      tc_fence_after();
-      const float inv_l = 1.f / lr;
-      const uint64_t inv_l2 = f2(inv_l, inv_l);
-      const bool live = q_idx < p.N;
-      const size_t row_off = (static_cast<size_t>(it.bh) * p.N + q_idx);
-      // this warp's first row; rows are D * 2 bytes apart
-      uint8_t *orow0 = reinterpret_cast<uint8_t *>(
-          static_cast<uint16_t *>(p.o) + (row_off - lane) * D);
-      const int rows_valid = p.N - (q_idx - static_cast<int>(lane));
-#pragma unroll
-      for (int half = 0; half < D / 64; ++half) {  // 64 columns = 128 bytes per row
-        uint4 v8[8];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t orr[32];
-          tmem_ld32(tO + 64 * half + 32 * c, orr);
-          tmem_ld_wait(orr);
-          uint32_t pk16[16];
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            float a, b;
-            f2_split(fmul2(f2(__uint_as_float(orr[2 * u]), __uint_as_float(orr[2 * u + 1])),
-                           inv_l2),
-                     a, b);
-            pk16[u] = pack2<BF16>(a, b);
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            v8[c * 4 + u] = make_uint4(pk16[4 * u], pk16[4 * u + 1], pk16[4 * u + 2],
-                                       pk16[4 * u + 3]);
-        }
-        store_rows<8>(v8, orow0 + 128 * half, static_cast<size_t>(D) * 2, rows_valid, lane);
-      }
-      if (live) p.lse[row_off] = (m + lg2_approx(l)) * 0.6931471805599453f;
-    }
-    tc_fence_before();
-    } else {
     // ------------------------------------------ softmax, column split
     // Two groups of eight warps, one per Q tile (warps 0-7: tile 0, 8-15:
     // tile 1), so the two tiles' softmax runs concurrently.  In a group,
@@ -1010,7 +821,6 @@ __global__ void __launch_bounds__(Cfg<D, BF16, SPLIT>::kThreads, 1)
       }
     }
     tc_fence_before();
-    }
   }
 
   __syncthreads();
