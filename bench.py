@@ -15,10 +15,11 @@ the kernel is launched on; the maximum over ranks is reported.  Q+K+V
 between steps.  Under torchrun each rank runs the same workload on its own
 GPU (heads are independent: weak scaling, no data-path collective).
 
-`e2e` repeats the measurement through the public API with pinned host
-buffers: every step copies Q, K, V host->device, runs the forward and
-copies O and LSE back, all inside the timed region (HostPipeline overlaps
-the copies of one chunk of heads with the forward of another).
+`e2e` repeats the measurement through the C ABI's host-buffer entry point
+(fa_fwd_host) with pinned host buffers: every step copies Q, K, V
+host->device, runs the forward and copies O and LSE back, all inside the
+timed region (the library overlaps the copies of one chunk of heads with
+the forward of another).
 
 `--impl reference` times the CPU oracle (the reference arm: a plain fp64
 C implementation of the definition) on the host cores, each step a bounded
@@ -322,20 +323,21 @@ def run_ours(args, w):
         raise RuntimeError(f"kernel status {status}: {fa.fa_strerror(status)}")
 
     # ------------------------------------------------ end to end, host buffers
-    # Pinned host Q, K, V in; pinned host O, LSE out; every step copies the
-    # inputs host->device, runs the forward and copies the outputs back, with
-    # the copies of one chunk of heads overlapping the forward of another
-    # (HostPipeline).  Timed on the host clock around fully synchronised steps.
+    # Pinned host Q, K, V in; pinned host O, LSE out; every step is one
+    # fa_fwd_host call, which copies the inputs host->device, runs the forward
+    # and copies the outputs back, with the copies of one chunk of heads
+    # overlapping the forward of another.  Timed on the host clock around
+    # fully synchronised steps.
     e2e = None
     if not args.no_e2e:
         pin = [x.pin_memory() for x in (q_h, k_h, v_h)]
         o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
         lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         n_e2e = max(1, min(args.steps, args.e2e_steps))
-        pipe = fa.HostPipeline(w.B, w.H, w.N, w.d, w.torch_dtype, dev, chunks=args.e2e_chunks)
+        n_chunks = max(1, min(args.e2e_chunks, w.B * w.H))
 
         def e2e_step():
-            pipe(*pin, o_h, lse_h, causal=w.causal)
+            fa.fa_fwd_host(*pin, o_h, lse_h, causal=w.causal, scale=w.scale, chunks=n_chunks)
 
         for _ in range(min(3, args.warmup) or 1):
             e2e_step()
@@ -352,9 +354,8 @@ def run_ours(args, w):
         d2h = o_h.numel() * o_h.element_size() + lse_h.numel() * lse_h.element_size()
         e2e = {"value": e2e_value, "unit": "TFLOPS",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
-               "ms_per_step": e2e_ms / n_e2e, "chunks": pipe.nchunks,
+               "ms_per_step": e2e_ms / n_e2e, "chunks": n_chunks, "api": "fa_fwd_host",
                "timing": "host clock around synchronised steps"}
-        del pipe
 
     if rank != 0:
         if world > 1:

@@ -16,7 +16,7 @@ import ctypes
 import math
 import os
 
-__all__ = ["FaError", "HostPipeline", "fa_fwd", "fa_fwd_fp16", "fa_fwd_ex", "fa_get_status",
+__all__ = ["FaError", "fa_fwd_host", "fa_fwd_noalloc", "fa_fwd", "fa_fwd_fp16", "fa_fwd_ex", "fa_get_status",
            "fa_strerror", "fa_version", "forward", "library_path", "lib"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -37,6 +37,8 @@ FA_ERR_OPTION = -11
 FA_ERR_SCRATCH = -12
 FA_MAX_N = 1 << 20
 FA_NOALLOC_SCRATCH_BYTES = 16 << 20
+FA_HOST_DEFAULT_CHUNKS = 8
+FA_HOST_MAX_CHUNKS = 1024
 FA_DEFAULT_RESCALE_THRESHOLD = 8.0
 FA_MAX_RESCALE_THRESHOLD = 12.0
 
@@ -75,6 +77,9 @@ def lib():
         L.fa_fwd_ex.restype = ctypes.c_int
         L.fa_fwd_noalloc.argtypes = L.fa_fwd_ex.argtypes
         L.fa_fwd_noalloc.restype = ctypes.c_int
+        L.fa_fwd_host.argtypes = [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int, ctypes.c_float,
+                                  ctypes.c_int, ctypes.c_int]
+        L.fa_fwd_host.restype = ctypes.c_int
         L.fa_selftest_wait_timeout.argtypes = [I64, P, P]
         L.fa_selftest_wait_timeout.restype = ctypes.c_int
         L.fa_get_status.argtypes = [P]
@@ -198,68 +203,35 @@ def forward(q, k, v, causal=False, scale=None, stream=None, rescale_threshold=No
     return o, lse
 
 
-class HostPipeline:
-    """Forward on pinned host buffers, pipelined over chunks of heads.
-
-    Every (batch, head) is independent, so the [B*H, N, d] tensors are cut
-    into chunks of heads.  Three in-order streams, one per engine: host ->
-    device copies, forwards (fa_fwd / fa_fwd_fp16 through the C ABI) and
-    device -> host copies, chained per chunk by events, so chunk c+1 loads
-    while chunk c computes and chunk c-1 drains.  Device staging buffers for
-    `depth` chunks are allocated once, here; each call synchronises at the
-    end.
-    """
-
-    def __init__(self, B, H, N, d, dtype, device=None, chunks=4, depth=3):
-        import torch
-        self.B, self.H, self.N, self.d = B, H, N, d
-        self.dtype = dtype
-        self.device = torch.device(device or "cuda")
-        bh = B * H
-        self.nchunks = max(1, min(int(chunks), bh))
-        self.bounds = [bh * c // self.nchunks for c in range(self.nchunks + 1)]
-        width = max(self.bounds[c + 1] - self.bounds[c] for c in range(self.nchunks))
-        self.depth = max(1, min(int(depth), self.nchunks))
-        self.bufs = []
-        for _ in range(self.depth):
-            mk = lambda: torch.empty((width, 1, N, d), dtype=dtype, device=self.device)
-            self.bufs.append(dict(q=mk(), k=mk(), v=mk(), o=mk(),
-                                  lse=torch.empty((width, 1, N), dtype=torch.float32,
-                                                  device=self.device)))
-        self.s_in = torch.cuda.Stream(self.device)
-        self.s_cp = torch.cuda.Stream(self.device)
-        self.s_out = torch.cuda.Stream(self.device)
-
-    def __call__(self, q, k, v, o, lse, causal=False, scale=None):
-        """q, k, v, o: pinned CPU [B,H,N,d]; lse: pinned CPU [B,H,N] fp32."""
-        import torch
-        bh, N, d = self.B * self.H, self.N, self.d
-        qf, kf, vf, of = (x.view(bh, 1, N, d) for x in (q, k, v, o))
-        lf = lse.view(bh, 1, N)
-        fn = fa_fwd if self.dtype == torch.bfloat16 else fa_fwd_fp16
-        free = [None] * self.depth  # buffer i drained to the host
-        for c in range(self.nchunks):
-            a, b = self.bounds[c], self.bounds[c + 1]
-            n = b - a
-            i = c % self.depth
-            buf = self.bufs[i]
-            if free[i] is not None:
-                self.s_in.wait_event(free[i])
-            with torch.cuda.stream(self.s_in):
-                for name, src in (("q", qf), ("k", kf), ("v", vf)):
-                    buf[name][:n].copy_(src[a:b], non_blocking=True)
-                loaded = torch.cuda.Event()
-                loaded.record(self.s_in)
-            self.s_cp.wait_event(loaded)
-            with torch.cuda.stream(self.s_cp):
-                fn(buf["q"][:n], buf["k"][:n], buf["v"][:n], buf["o"][:n], buf["lse"][:n],
-                   causal=causal, scale=scale, stream=self.s_cp)
-                done = torch.cuda.Event()
-                done.record(self.s_cp)
-            self.s_out.wait_event(done)
-            with torch.cuda.stream(self.s_out):
-                of[a:b].copy_(buf["o"][:n], non_blocking=True)
-                lf[a:b].copy_(buf["lse"][:n], non_blocking=True)
-                free[i] = torch.cuda.Event()
-                free[i].record(self.s_out)
-        self.s_out.synchronize()
+def fa_fwd_host(q, k, v, o, lse, causal=False, scale=None, chunks=0) -> None:
+    """Forward on HOST tensors through the C ABI (fa_fwd_host): q, k, v, o
+    [B,H,N,d] bf16/fp16 and lse [B,H,N] fp32, contiguous CPU tensors
+    (pinned for full copy speed).  The library pipelines the copies and the
+    kernels over `chunks` groups of heads (0 = its default) and returns when
+    o and lse are written."""
+    import torch
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"unsupported dtype {q.dtype}: use bfloat16 or float16")
+    B, H, N, d = q.shape
+    for name, t, dt, shape in (("q", q, q.dtype, (B, H, N, d)), ("k", k, q.dtype, (B, H, N, d)),
+                               ("v", v, q.dtype, (B, H, N, d)), ("o", o, q.dtype, (B, H, N, d)),
+                               ("lse", lse, torch.float32, (B, H, N))):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.is_cuda:
+            raise ValueError(f"{name} must be a host (CPU) tensor")
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc = lib().fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           B, H, N, d, int(bool(causal)), float(scale),
+                           int(q.dtype == torch.float16), int(chunks))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_host")

@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -26,6 +27,10 @@ struct DeviceState {
   unsigned *status = nullptr;  // device address of g_fa_status
   cudaMemPool_t pool = nullptr;  // stream-ordered scratch for split items (none: no split)
   uint8_t *noalloc = nullptr;    // device address of g_fa_noalloc_scratch
+  // fa_fwd_host: copy-in, compute and copy-out streams (created on first use)
+  std::once_flag host_once;
+  int host_err = FA_OK;
+  cudaStream_t s_in = nullptr, s_cp = nullptr, s_out = nullptr;
   std::once_flag attr_once[4];
   int attr_err[4] = {0, 0, 0, 0};
 };
@@ -305,6 +310,115 @@ int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *
                    float rescale_threshold, fa_stream_t stream) {
   return fwd_common(fp16 == 0, q, k, v, o, lse, B, H, N, d, causal, scale, rescale_threshold,
                     stream, /*noalloc=*/true);
+}
+
+// Pipelined forward on host buffers: heads in chunks; chunk c+1 is copied
+// in on s_in while chunk c is computed on s_cp and chunk c-1 is copied out on
+// s_out, through `depth` rotating device staging buffers taken from the pool.
+int fa_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                int64_t H, int64_t N, int64_t d, int causal, float scale, int fp16,
+                int chunks) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (N > FA_MAX_N) return FA_ERR_UNSUPPORTED_N;
+  const int64_t kLimit = int64_t(1) << 40;
+  if (B > kLimit / H || B * H > kLimit / N || B * H * N > kLimit / d) return FA_ERR_SHAPE;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+  if (chunks < 0 || chunks > FA_HOST_MAX_CHUNKS) return FA_ERR_OPTION;
+  const int64_t BH = B * H;
+  const size_t head_bytes = static_cast<size_t>(N * d) * 2, head_lse = static_cast<size_t>(N) * 4;
+  const size_t tbytes = head_bytes * BH, lbytes = head_lse * BH;
+  for (const void *in : {q, k, v})
+    if (overlaps(o, tbytes, in, tbytes) || overlaps(lse, lbytes, in, tbytes)) return FA_ERR_ALIAS;
+  if (overlaps(o, tbytes, lse, lbytes)) return FA_ERR_ALIAS;
+
+  DeviceState *ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != FA_OK) return rc;
+  std::call_once(ds->host_once, [&] {
+    for (cudaStream_t *st : {&ds->s_in, &ds->s_cp, &ds->s_out}) {
+      cudaError_t e = cudaStreamCreateWithFlags(st, cudaStreamNonBlocking);
+      if (e != cudaSuccess) {
+        t_last_cuda_error = static_cast<int>(e);
+        ds->host_err = FA_ERR_CUDA;
+        return;
+      }
+    }
+  });
+  if (ds->host_err != FA_OK) return ds->host_err;
+
+  const int64_t nch = std::min<int64_t>(chunks == 0 ? FA_HOST_DEFAULT_CHUNKS : chunks, BH);
+  int64_t width = 0;
+  for (int64_t c = 0; c < nch; ++c)
+    width = std::max(width, BH * (c + 1) / nch - BH * c / nch);
+  const int depth = static_cast<int>(std::min<int64_t>(3, nch));
+  // q, k, v, o, lse of one chunk; slots start on 256-byte boundaries
+  const size_t slot_bytes = (4 * head_bytes * width + head_lse * width + 255) & ~size_t(255);
+  cudaEvent_t ev[3][3] = {};  // [slot][loaded, done, drained]
+  uint8_t *stage = nullptr;
+  cudaError_t e = cudaSuccess;
+  auto fail = [&](cudaError_t err) {
+    rc = cuda_fail(err);
+  };
+  for (int i = 0; i < depth && rc == FA_OK; ++i)
+    for (int j = 0; j < 3 && rc == FA_OK; ++j)
+      if ((e = cudaEventCreateWithFlags(&ev[i][j], cudaEventDisableTiming)) != cudaSuccess) fail(e);
+  if (rc == FA_OK) {
+    void *mem = nullptr;
+    e = ds->pool ? cudaMallocFromPoolAsync(&mem, slot_bytes * depth, ds->pool, ds->s_in)
+                 : cudaMallocAsync(&mem, slot_bytes * depth, ds->s_in);
+    if (e != cudaSuccess) fail(e);
+    stage = static_cast<uint8_t *>(mem);
+  }
+  const uint8_t *qh = static_cast<const uint8_t *>(q), *kh = static_cast<const uint8_t *>(k),
+                *vh = static_cast<const uint8_t *>(v);
+  uint8_t *oh = static_cast<uint8_t *>(o), *lh = reinterpret_cast<uint8_t *>(lse);
+  for (int64_t c = 0; c < nch && rc == FA_OK; ++c) {
+    const int64_t a = BH * c / nch, n = BH * (c + 1) / nch - a;
+    const int i = static_cast<int>(c % depth);
+    uint8_t *sq = stage + slot_bytes * i, *sk = sq + head_bytes * width,
+            *sv = sk + head_bytes * width, *so = sv + head_bytes * width,
+            *sl = so + head_bytes * width;
+    const size_t tb = head_bytes * n, off = head_bytes * a;
+    if (c >= depth && (e = cudaStreamWaitEvent(ds->s_in, ev[i][2], 0)) != cudaSuccess) { fail(e); break; }
+    if ((e = cudaMemcpyAsync(sq, qh + off, tb, cudaMemcpyHostToDevice, ds->s_in)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(sk, kh + off, tb, cudaMemcpyHostToDevice, ds->s_in)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(sv, vh + off, tb, cudaMemcpyHostToDevice, ds->s_in)) != cudaSuccess ||
+        (e = cudaEventRecord(ev[i][0], ds->s_in)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(ds->s_cp, ev[i][0], 0)) != cudaSuccess) {
+      fail(e);
+      break;
+    }
+    rc = fwd_common(fp16 == 0, sq, sk, sv, so, reinterpret_cast<float *>(sl), n, 1, N, d, causal,
+                    scale, FA_DEFAULT_RESCALE_THRESHOLD, ds->s_cp);
+    if (rc != FA_OK) break;
+    if ((e = cudaEventRecord(ev[i][1], ds->s_cp)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(ds->s_out, ev[i][1], 0)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(oh + off, so, tb, cudaMemcpyDeviceToHost, ds->s_out)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(lh + head_lse * a, sl, head_lse * n, cudaMemcpyDeviceToHost,
+                             ds->s_out)) != cudaSuccess ||
+        (e = cudaEventRecord(ev[i][2], ds->s_out)) != cudaSuccess) {
+      fail(e);
+      break;
+    }
+  }
+  // Everything queued so far finishes before the staging memory is given
+  // back (s_out's last copy waits for the last forward, which waits for the
+  // last copy in), and before the call returns.
+  for (cudaStream_t st : {ds->s_in, ds->s_cp, ds->s_out}) {
+    cudaError_t es = cudaStreamSynchronize(st);
+    if (es != cudaSuccess && rc == FA_OK) fail(es);
+  }
+  if (stage != nullptr) {
+    cudaFreeAsync(stage, ds->s_out);
+    cudaError_t es = cudaStreamSynchronize(ds->s_out);
+    if (es != cudaSuccess && rc == FA_OK) fail(es);
+  }
+  for (int i = 0; i < 3; ++i)
+    for (int j = 0; j < 3; ++j)
+      if (ev[i][j]) cudaEventDestroy(ev[i][j]);
+  return rc;
 }
 
 int fa_selftest_wait_timeout(int64_t timeout_us, int *gave_up, fa_stream_t stream) {

@@ -147,6 +147,36 @@ int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *
                    int64_t H, int64_t N, int64_t d, int causal, float scale, int fp16,
                    float rescale_threshold, fa_stream_t stream);
 
+/* Work split of fa_fwd_host. */
+#define FA_HOST_DEFAULT_CHUNKS 8
+#define FA_HOST_MAX_CHUNKS 1024
+
+/*
+ * fa_fwd_host -- the forward on HOST buffers.
+ *
+ * q, k, v are read from, and o, lse written to, host memory in the layout
+ * above (page-locked memory -- cudaHostAlloc, cudaHostRegister -- for full
+ * copy speed; pageable memory works, staged by the driver).  The B*H heads
+ * are processed in `chunks` groups (0 = FA_HOST_DEFAULT_CHUNKS, at most
+ * FA_HOST_MAX_CHUNKS, at most B*H): while chunk c is computed, chunk c+1 is
+ * copied to the device and chunk c-1 back to the host, on three streams of
+ * the library's own, through three rotating device staging buffers taken
+ * from the library's memory pool for the call.  Every chunk is one fa_fwd_ex
+ * launch with the default rescale threshold.  The call returns when o and
+ * lse are written; it does not wait for, or order itself after, work on
+ * other streams.
+ *
+ *   fp16   : 0 = bf16 q/k/v/o, 1 = fp16
+ *   chunks : see above; out of range gives FA_ERR_OPTION
+ *
+ * Errors are fa_fwd's (alignment is not required of host pointers); a CUDA
+ * failure during the pipeline gives FA_ERR_CUDA, and o/lse may then be
+ * partly written.  A pipeline wait that gave up is reported by
+ * fa_get_status, as for fa_fwd.
+ */
+int fa_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                int64_t H, int64_t N, int64_t d, int causal, float scale, int fp16, int chunks);
+
 /*
  * fa_get_status -- synchronises `stream`, then returns and clears the
  * current device's status word: FA_OK, or FA_ERR_TIMEOUT if some launch

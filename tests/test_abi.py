@@ -122,6 +122,25 @@ def test_fa_fwd_noalloc_argument_errors(lib):
     assert "FA_NOALLOC_SCRATCH_BYTES" in lib.fa_strerror(fa.FA_ERR_SCRATCH).decode()
 
 
+def test_fa_fwd_host_argument_errors(lib):
+    """The host-buffer entry point checks its arguments before touching the
+    device (host pointers need no alignment)."""
+    def h(chunks=0, **kw):
+        a = dict(q=Q, k=K, v=V, o=O, lse=L, B=1, H=1, N=128, d=128, causal=0, scale=0.125,
+                 fp16=0)
+        a.update(kw)
+        return lib.fa_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
+                               a["d"], a["causal"], a["scale"], a["fp16"], chunks)
+    assert h(q=None) == fa.FA_ERR_NULL
+    assert h(B=0) == fa.FA_ERR_SHAPE
+    assert h(d=32) == fa.FA_ERR_HEADDIM
+    assert h(N=fa.FA_MAX_N + 1) == fa.FA_ERR_UNSUPPORTED_N
+    assert h(scale=float("nan")) == fa.FA_ERR_SCALE
+    assert h(chunks=-1) == fa.FA_ERR_OPTION
+    assert h(chunks=fa.FA_HOST_MAX_CHUNKS + 1) == fa.FA_ERR_OPTION
+    assert h(o=Q) == fa.FA_ERR_ALIAS
+
+
 def test_selftest_argument_errors(lib):
     assert lib.fa_selftest_wait_timeout(1000, None, None) == fa.FA_ERR_NULL
     assert lib.fa_selftest_wait_timeout(0, 0x10000000, None) == fa.FA_ERR_OPTION

@@ -267,21 +267,37 @@ def test_bounded_wait_gives_up_and_context_survives():
     assert_close(o, lse, o_ref, lse_ref, "after timeout self-test")
 
 
-@pytest.mark.parametrize("chunks,depth", [(1, 1), (3, 2), (5, 3)])
-def test_host_pipeline_matches_oracle(chunks, depth):
-    """The pipelined host-buffer forward (chunks of heads on several streams)
-    gives the oracle's result, twice in a row with reused staging buffers."""
+@pytest.mark.parametrize("chunks", [1, 3, 5, 0])
+def test_fa_fwd_host_matches_oracle(chunks):
+    """The pipelined host-buffer forward (fa_fwd_host: chunks of heads, copies
+    and kernels on the library's three streams) gives the oracle's result,
+    twice in a row (staging memory taken from the pool again)."""
     B, H, N, d = 2, 5, 333, 128
     q, k, v = make_qkv(B, H, N, d, torch.bfloat16, seed=40)
     pin = [x.pin_memory() for x in (q, k, v)]
-    pipe = fa().HostPipeline(B, H, N, d, torch.bfloat16, "cuda", chunks=chunks, depth=depth)
     for causal in (True, False):
         o = torch.empty_like(q).pin_memory()
         lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-        pipe(*pin, o, lse, causal=causal)
+        fa().fa_fwd_host(*pin, o, lse, causal=causal, chunks=chunks)
         assert fa().fa_get_status() == 0
         o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 1.0 / math.sqrt(d))
-        assert_close(o.float().numpy(), lse.numpy(), o_ref, lse_ref, f"pipeline {chunks}/{depth}")
+        assert_close(o.float().numpy(), lse.numpy(), o_ref, lse_ref, f"host chunks={chunks}")
+
+
+def test_fa_fwd_host_pageable_fp16_and_bitwise():
+    """Pageable (not pinned) fp16 host buffers, d = 64, a chunk count above
+    B*H (clamped): the same bits as fa_fwd_ex on device copies of the inputs."""
+    B, H, N, d = 1, 3, 1000, 64
+    q, k, v = make_qkv(B, H, N, d, torch.float16, seed=41)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32)
+    fa().fa_fwd_host(q, k, v, o, lse, causal=False, chunks=7)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    od = torch.empty_like(qd)
+    ld = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    fa().fa_fwd_ex(qd, kd, vd, od, ld, causal=False)
+    torch.cuda.synchronize()
+    assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
 
 
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
