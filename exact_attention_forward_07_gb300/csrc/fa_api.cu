@@ -27,10 +27,16 @@ struct DeviceState {
   unsigned *status = nullptr;  // device address of g_fa_status
   cudaMemPool_t pool = nullptr;  // stream-ordered scratch for split items (none: no split)
   uint8_t *noalloc = nullptr;    // device address of g_fa_noalloc_scratch
-  // fa_fwd_host: copy-in, compute and copy-out streams (created on first use)
+  // fa_fwd_host: copy-in, compute and copy-out streams, events and device
+  // staging memory (created on first use, staging grown as needed); calls
+  // on one device take host_mu, so they run one at a time
   std::once_flag host_once;
   int host_err = FA_OK;
+  std::mutex host_mu;
   cudaStream_t s_in = nullptr, s_cp = nullptr, s_out = nullptr;
+  cudaEvent_t host_ev[3][3] = {};  // [slot][loaded, done, drained]
+  uint8_t *stage = nullptr;
+  size_t stage_bytes = 0;
   std::once_flag attr_once[4];
   int attr_err[4] = {0, 0, 0, 0};
 };
@@ -345,8 +351,18 @@ int fa_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse
         return;
       }
     }
+    for (int i = 0; i < 3; ++i)
+      for (int j = 0; j < 3; ++j) {
+        cudaError_t e = cudaEventCreateWithFlags(&ds->host_ev[i][j], cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+          t_last_cuda_error = static_cast<int>(e);
+          ds->host_err = FA_ERR_CUDA;
+          return;
+        }
+      }
   });
   if (ds->host_err != FA_OK) return ds->host_err;
+  std::lock_guard<std::mutex> lock(ds->host_mu);
 
   const int64_t nch = std::min<int64_t>(chunks == 0 ? FA_HOST_DEFAULT_CHUNKS : chunks, BH);
   int64_t width = 0;
@@ -355,22 +371,19 @@ int fa_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse
   const int depth = static_cast<int>(std::min<int64_t>(3, nch));
   // q, k, v, o, lse of one chunk; slots start on 256-byte boundaries
   const size_t slot_bytes = (4 * head_bytes * width + head_lse * width + 255) & ~size_t(255);
-  cudaEvent_t ev[3][3] = {};  // [slot][loaded, done, drained]
-  uint8_t *stage = nullptr;
+  cudaEvent_t(&ev)[3][3] = ds->host_ev;
   cudaError_t e = cudaSuccess;
-  auto fail = [&](cudaError_t err) {
-    rc = cuda_fail(err);
-  };
-  for (int i = 0; i < depth && rc == FA_OK; ++i)
-    for (int j = 0; j < 3 && rc == FA_OK; ++j)
-      if ((e = cudaEventCreateWithFlags(&ev[i][j], cudaEventDisableTiming)) != cudaSuccess) fail(e);
-  if (rc == FA_OK) {
+  auto fail = [&](cudaError_t err) { rc = cuda_fail(err); };
+  if (ds->stage_bytes < slot_bytes * depth) {  // grow the staging memory (all streams idle)
+    if (ds->stage != nullptr) cudaFree(ds->stage);
+    ds->stage = nullptr;
+    ds->stage_bytes = 0;
     void *mem = nullptr;
-    e = ds->pool ? cudaMallocFromPoolAsync(&mem, slot_bytes * depth, ds->pool, ds->s_in)
-                 : cudaMallocAsync(&mem, slot_bytes * depth, ds->s_in);
-    if (e != cudaSuccess) fail(e);
-    stage = static_cast<uint8_t *>(mem);
+    if ((e = cudaMalloc(&mem, slot_bytes * depth)) != cudaSuccess) return cuda_fail(e);
+    ds->stage = static_cast<uint8_t *>(mem);
+    ds->stage_bytes = slot_bytes * depth;
   }
+  uint8_t *stage = ds->stage;
   const uint8_t *qh = static_cast<const uint8_t *>(q), *kh = static_cast<const uint8_t *>(k),
                 *vh = static_cast<const uint8_t *>(v);
   uint8_t *oh = static_cast<uint8_t *>(o), *lh = reinterpret_cast<uint8_t *>(lse);
@@ -403,21 +416,15 @@ int fa_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse
       break;
     }
   }
-  // Everything queued so far finishes before the staging memory is given
-  // back (s_out's last copy waits for the last forward, which waits for the
-  // last copy in), and before the call returns.
-  for (cudaStream_t st : {ds->s_in, ds->s_cp, ds->s_out}) {
-    cudaError_t es = cudaStreamSynchronize(st);
-    if (es != cudaSuccess && rc == FA_OK) fail(es);
+  // s_out's last copy waits for the last forward, which waits for the last
+  // copy in: on success that one stream covers all the work.  After a
+  // failure part of the pipeline may not be chained, so all three are
+  // drained before the staging memory can be reused.
+  if (rc == FA_OK) {
+    if ((e = cudaStreamSynchronize(ds->s_out)) != cudaSuccess) fail(e);
+  } else {
+    for (cudaStream_t st : {ds->s_in, ds->s_cp, ds->s_out}) cudaStreamSynchronize(st);
   }
-  if (stage != nullptr) {
-    cudaFreeAsync(stage, ds->s_out);
-    cudaError_t es = cudaStreamSynchronize(ds->s_out);
-    if (es != cudaSuccess && rc == FA_OK) fail(es);
-  }
-  for (int i = 0; i < 3; ++i)
-    for (int j = 0; j < 3; ++j)
-      if (ev[i][j]) cudaEventDestroy(ev[i][j]);
   return rc;
 }
 

@@ -63,7 +63,7 @@ struct Params {
   int causal;
   float scale_log2;  // scale * log2(e)
   float rescale_thr; // rescale O only when the running max grows by more than this (log2 units)
-  // Wave-tail split (non-causal, column-split kernel only): the items from
+  // Wave-tail split (non-causal only): the items from
   // split_first on (those of the last, partial round of the persistent
   // grid) are cut into split_k pieces along the key blocks; each piece
   // leaves its O (normalised by its own sum) and row statistics in scratch

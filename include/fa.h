@@ -20,10 +20,11 @@
  * current CUDA device.
  *
  * Ownership: the caller allocates and owns q, k, v, o and lse.  Non-causal
- * d = 128 calls whose last round of work items is split along the keys (the
+ * calls whose last round of work items is split along the keys (the
  * wave-tail split: when fewer than half the SMs would have an item in the
  * last round) take scratch memory for the pieces' partial results -- at
- * most one piece per SM, 131 KiB each, plus 4 bytes per split item -- from
+ * most one piece per SM, 1 KiB * d + 3 KiB each, plus 4 bytes per split
+ * item -- from
  * a stream-ordered memory pool the library creates per device; it is
  * returned to the pool behind the kernel on the same stream, and the pool
  * keeps its memory, so after the first such call no device allocation
@@ -131,11 +132,12 @@ int fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, 
  * from one fixed array of FA_NOALLOC_SCRATCH_BYTES in the library's device
  * memory, located once per device (cudaGetSymbolAddress) when the library
  * first sets the device up, instead of from the memory pool.  A call whose
- * split needs more than that -- 134,144 bytes per piece (d = 128) plus 4 per
- * split item, so at most 125 pieces; e.g. the 144 pieces of a non-causal
- * [8,16,4096,128] call on 152 SMs -- is rejected with FA_ERR_SCRATCH before
- * anything is launched (o and lse are not written); fa_fwd_ex serves it.
- * Calls that need no scratch (causal, d = 64, or a last round that is not
+ * split needs more than that -- 1024 * d + 3072 bytes per piece plus 4 per
+ * split item, so at most 125 pieces at d = 128; e.g. the 144 pieces of a
+ * non-causal [8,16,4096,128] call on 152 SMs -- is rejected with
+ * FA_ERR_SCRATCH before anything is launched (o and lse are not written);
+ * fa_fwd_ex serves it.
+ * Calls that need no scratch (causal, or a last round that is not
  * split) are always accepted, and the rest give bitwise fa_fwd_ex's result.
  *
  * The array is shared by every fa_fwd_noalloc call on the device, so these
@@ -160,11 +162,12 @@ int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *
  * are processed in `chunks` groups (0 = FA_HOST_DEFAULT_CHUNKS, at most
  * FA_HOST_MAX_CHUNKS, at most B*H): while chunk c is computed, chunk c+1 is
  * copied to the device and chunk c-1 back to the host, on three streams of
- * the library's own, through three rotating device staging buffers taken
- * from the library's memory pool for the call.  Every chunk is one fa_fwd_ex
- * launch with the default rescale threshold.  The call returns when o and
- * lse are written; it does not wait for, or order itself after, work on
- * other streams.
+ * the library's own, through three rotating device staging buffers (kept by
+ * the library per device, grown to the largest call seen).  Every chunk is
+ * one fa_fwd_ex launch with the default rescale threshold.  The call returns
+ * when o and lse are written; it does not wait for, or order itself after,
+ * work on other streams.  Calls on one device from several host threads run
+ * one at a time.
  *
  *   fp16   : 0 = bf16 q/k/v/o, 1 = fp16
  *   chunks : see above; out of range gives FA_ERR_OPTION
