@@ -66,6 +66,10 @@ WORKLOADS = {
                                        True, index=3),
     "b16h32n8192d128_fp16_peaked": Workload("b16h32n8192d128_fp16_peaked", 16, 32, 8192, 128,
                                             "fp16", False, k_mult=4.0, index=4),
+    # the same per-head shape and values with 1/8 of the heads (0.5 GiB on the
+    # device): a case small enough for a full profiler capture
+    "b2h32n8192d128_fp16_peaked": Workload("b2h32n8192d128_fp16_peaked", 2, 32, 8192, 128,
+                                           "fp16", False, k_mult=4.0, index=4),
 }
 
 BASE_SEED = 0
