@@ -214,9 +214,24 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
       const size_t bytes_cnt = static_cast<size_t>(R) * sizeof(unsigned);
       const size_t need = bytes_o + bytes_st + bytes_cnt;
       uint8_t *base = nullptr;
+      // Under stream capture the scratch becomes a graph allocation
+      // (cudaMallocAsync, freed by the graph behind the kernel) instead of
+      // pool memory, so that capturing the call never breaks the capture.
+      cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+      if (!noalloc && cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        cap = cudaStreamCaptureStatusInvalidated;
+      }
       if (noalloc) {
         if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_SCRATCH;
         base = ds.noalloc;
+      } else if (cap == cudaStreamCaptureStatusActive) {
+        if (cudaMallocAsync(&scratch, need, stream) == cudaSuccess)
+          base = static_cast<uint8_t *>(scratch);
+        else
+          scratch = nullptr;  // the capture reports its own error
+      } else if (cap != cudaStreamCaptureStatusNone) {
+        // capture state unknown: run unsplit, touching no allocator
       } else if (cudaMallocFromPoolAsync(&scratch, need, ds.pool, stream) != cudaSuccess) {
         // a failed scratch allocation only means no split (its error is cleared)
         scratch = nullptr;

@@ -196,6 +196,30 @@ def test_deterministic_bitwise():
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("B,H,N,causal", [(1, 2, 4096, False), (2, 4, 1000, True)],
+                         ids=["split", "causal"])
+def test_cuda_graph_capture_replays_bitwise(B, H, N, causal):
+    """fa_fwd captured into a CUDA graph replays to the eager result bit for
+    bit, twice: launches inside stream capture work, and the wave-tail
+    split's scratch (here 128 pieces) becomes a graph allocation."""
+    dev = torch.device("cuda")
+    q, k, v = (x.to(dev) for x in make_qkv(B, H, N, 128, torch.bfloat16, seed=14))
+    o_ref, l_ref = fa().forward(q, k, v, causal=causal)
+    torch.cuda.synchronize()
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fa().fa_fwd(q, k, v, o, lse, causal=causal)
+    for _ in range(2):
+        o.zero_()
+        lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+    assert fa().fa_get_status() == 0
+
+
 def test_side_stream_and_explicit_scale():
     q, k, v = make_qkv(1, 2, 700, 64, torch.bfloat16, seed=10)
     s = torch.cuda.Stream()
