@@ -34,7 +34,10 @@
  * overlap q, k, v or each other.
  *
  * Execution: asynchronous on `stream` (0 = legacy default stream); no host
- * synchronisation.  Safe to call from several host threads.
+ * synchronisation.  Safe to call from several host threads.  fa_fwd,
+ * fa_fwd_fp16, fa_fwd_ex and fa_fwd_noalloc may be captured into a CUDA
+ * graph (stream capture): the split schedule's scratch then becomes a graph
+ * allocation (cudaMallocAsync / cudaFreeAsync nodes) instead of pool memory.
  *
  * Errors: 0 on success, a negative FA_ERR_* code otherwise.  On an argument
  * error nothing is launched and o/lse are not written.  Faults seen while
