@@ -220,6 +220,28 @@ def test_cuda_graph_capture_replays_bitwise(B, H, N, causal):
     assert fa().fa_get_status() == 0
 
 
+def test_concurrent_streams_split_scratch():
+    """Calls on two streams at once, each with a split last round, take
+    separate scratch from the stream-ordered pool: both match their serial
+    results bit for bit."""
+    dev = torch.device("cuda")
+    a = [x.to(dev) for x in make_qkv(1, 2, 4096, 128, torch.bfloat16, seed=15)]
+    b = [x.to(dev) for x in make_qkv(1, 3, 2048, 128, torch.bfloat16, seed=16)]
+    ref_a = fa().forward(*a, causal=False)
+    ref_b = fa().forward(*b, causal=False)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            oa = fa().forward(*a, causal=False, stream=s1)
+        with torch.cuda.stream(s2):
+            ob = fa().forward(*b, causal=False, stream=s2)
+        torch.cuda.synchronize()
+        assert torch.equal(oa[0], ref_a[0]) and torch.equal(oa[1], ref_a[1])
+        assert torch.equal(ob[0], ref_b[0]) and torch.equal(ob[1], ref_b[1])
+    assert fa().fa_get_status() == 0
+
+
 def test_side_stream_and_explicit_scale():
     q, k, v = make_qkv(1, 2, 700, 64, torch.bfloat16, seed=10)
     s = torch.cuda.Stream()
