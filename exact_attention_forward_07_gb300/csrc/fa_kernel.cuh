@@ -5,8 +5,9 @@
 // tile 1 = the next 128 rows.  This is the query-block parallelism of the
 // FlashAttention v2 work-partitioning diagram (pseudo-code panel, "parallel
 // for batch, head, q_block"; core panel item 2: more CTAs along the
-// sequence) and its sliced-Q split (each softmax warp owns 32 Q rows; K/V
-// tiles are shared and no warp reduces another's output).
+// sequence) and its sliced-Q split (each softmax warp owns 32 Q rows and
+// half of their S columns; K/V tiles are shared, and the only exchange
+// between warps is a row maximum and a row sum between the two halves).
 //
 // Roles inside the CTA (FlashAttention v4 Blackwell pipeline diagram, the
 // producer / MMA / softmax lanes and the pseudo-code panel), 640 threads:
