@@ -163,6 +163,36 @@ def test_parity_wave_tail_split(B, H, N, dtype):
     assert_close(o, lse, o_ref, lse_ref, f"split {B},{H},{N},{dtype}")
 
 
+def _random_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        d = int(rng.choice([64, 128]))
+        N = int(rng.integers(1, 1500))
+        B = int(rng.integers(1, 4))
+        H = int(rng.integers(1, 5))
+        causal = bool(rng.integers(0, 2))
+        dtype = torch.bfloat16 if rng.integers(0, 2) else torch.float16
+        cases.append((B, H, N, d, causal, dtype))
+    return cases
+
+
+RANDOM_CASES = _random_cases(32, seed=2026)
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,dtype", RANDOM_CASES,
+                         ids=[f"b{b}h{h}n{n}d{d}-{'c' if c else 'f'}-{str(t)[6:]}"
+                              for b, h, n, d, c, t in RANDOM_CASES])
+def test_parity_random_shapes(B, H, N, d, causal, dtype):
+    """Seeded random shapes (any N up to 1500, both head dims, both masks,
+    both dtypes; many of them hit the wave-tail split, ragged tails and odd
+    tile counts), full tensors against the oracle."""
+    q, k, v = make_qkv(B, H, N, d, dtype, seed=1000 + N * 7 + d + B * 3 + H)
+    o, lse = run_gpu(q, k, v, causal)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 1.0 / math.sqrt(d))
+    assert_close(o, lse, o_ref, lse_ref, f"{B},{H},{N},{d},causal={causal},{dtype}")
+
+
 def test_wave_tail_split_peaked_rows():
     """Pieces of one row see very different maxima (K scaled x6, sorted so
     the largest logits sit in the last piece): the merge must weigh each
