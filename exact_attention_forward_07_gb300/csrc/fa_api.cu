@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "fa.h"
 #include "fa_kernel.cuh"
@@ -154,6 +155,38 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
+// Causal item order.  In round r of the static schedule CTA b takes item
+// r * G + b (even rounds) or r * G + G - 1 - b (odd rounds).  Taking the
+// heaviest pairs first across all heads balances the SMs best, but once the
+// heads' K/V outgrow L2 it reads a head's K/V from HBM again for each of its
+// pairs; head by head (heaviest pair first within each head) keeps a head's
+// K/V in L2 across its pairs.  Both orders' per-CTA load is simulated (the
+// larger tile's K/V blocks per item, plus about 1.3 blocks for the restart
+// between items) and head by head is taken when it balances within half a
+// percent of the other.  Large launches (over 2^20 items) keep the first order.
+bool causal_head_major(int BH, int n_qtiles, int n_pairs, int G) {
+  const int64_t n = static_cast<int64_t>(BH) * n_pairs;
+  if (n <= G || n > (int64_t(1) << 20)) return false;
+  std::vector<double> load(static_cast<size_t>(G));
+  auto balance = [&](bool head_major) {
+    std::fill(load.begin(), load.end(), 0.0);
+    for (int64_t i = 0; i < n; ++i) {
+      const int64_t r = i / G, off = i - r * G;
+      const int64_t b = (r & 1) ? G - 1 - off : off;
+      const int64_t level = head_major ? i % n_pairs : i / BH;
+      const int64_t qt1 = 2 * (n_pairs - 1 - level) + 1;
+      load[static_cast<size_t>(b)] += static_cast<double>(qt1 < n_qtiles ? qt1 + 1 : qt1) + 1.3;
+    }
+    double sum = 0.0, mx = 0.0;
+    for (double x : load) {
+      sum += x;
+      mx = std::max(mx, x);
+    }
+    return sum / G / mx;
+  };
+  return balance(true) >= balance(false) - 0.005;
+}
+
 template <int D, bool BF16>
 int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *v, void *o,
            float *lse, int64_t BH, int64_t N, int causal, float scale, float thr, bool noalloc,
@@ -183,6 +216,12 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
   p.n_pairs = (p.n_qtiles + 1) / 2;
   p.n_items = p.BH * p.n_pairs;
   p.causal = causal ? 1 : 0;
+  // K and V of all heads beyond 64 MiB: L2 (126 MB) no longer holds them
+  const double kv_bytes = 2.0 * static_cast<double>(BH) * static_cast<double>(N) * D * 2.0;
+  p.causal_head_major = causal && kv_bytes > 64.0 * 1024 * 1024 &&
+                                causal_head_major(p.BH, p.n_qtiles, p.n_pairs, ds.sm_count)
+                            ? 1
+                            : 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.rescale_thr = thr;
 

@@ -62,6 +62,7 @@ struct Params {
   int n_pairs;       // ceil(n_qtiles / 2)
   int n_items;       // BH * n_pairs
   int causal;
+  int causal_head_major;  // causal item order: 0 heaviest pair first across heads, 1 head by head
   float scale_log2;  // scale * log2(e)
   float rescale_thr; // rescale O only when the running max grows by more than this (log2 units)
   // Wave-tail split (non-causal only): the items from
@@ -122,11 +123,17 @@ struct Item {
 // Work item -> (head, first Q tile, K/V blocks for each of the two tiles).
 // Non-causal items run head-major so CTAs working at the same time share a
 // few heads' K/V in L2.  Causal items run heaviest pair first (the pair
-// nearest the end of the sequence sees the most keys).
+// nearest the end of the sequence sees the most keys), across all heads --
+// or, where the host found that order no better balanced, head by head
+// (heaviest pair first within a head), which keeps each head's K/V in L2
+// for all of its pairs.
 __device__ __forceinline__ Item decode_item(int item, const Params &p) {
   Item it;
   int pair;
-  if (p.causal) {
+  if (p.causal && p.causal_head_major) {
+    it.bh = item / p.n_pairs;
+    pair = p.n_pairs - 1 - (item - it.bh * p.n_pairs);
+  } else if (p.causal) {
     const int level = item / p.BH;
     it.bh = item - level * p.BH;
     pair = p.n_pairs - 1 - level;

@@ -110,6 +110,24 @@ def test_parity_large_workloads_sampled(name):
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
 
 
+def test_parity_causal_head_by_head_order():
+    """A causal launch whose K/V (128 MiB) outgrow L2 and whose static rounds
+    balance as well head by head as heaviest-pair-first, so the library takes
+    its items head by head: one seeded row of every (head, Q tile) is checked,
+    so a work item that went missing or to the wrong head cannot pass."""
+    B, H, N, d = 8, 64, 1024, 64
+    q, k, v = make_qkv(B, H, N, d, torch.bfloat16, seed=4242)
+    o, lse = run_gpu(q, k, v, True)
+    BH, tiles = B * H, N // 128
+    rng = np.random.default_rng(11)
+    rows = np.array([h * N + t * 128 + int(rng.integers(0, 128))
+                     for h in range(BH) for t in range(tiles)], dtype=np.int64)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, True, 1.0 / math.sqrt(d), rows=rows)
+    assert_close(o.reshape(BH * N, d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref,
+                 "causal [8,64,1024,64] head by head")
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+
+
 def test_uniform_attention_q_zero():
     """Q = 0: every visible key gets the same weight (closed form)."""
     q, k, v = make_qkv(1, 2, 300, 128, torch.bfloat16, seed=5, q_zero=True)
