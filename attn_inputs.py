@@ -70,6 +70,10 @@ WORKLOADS = {
     # device): a case small enough for a full profiler capture
     "b2h32n8192d128_fp16_peaked": Workload("b2h32n8192d128_fp16_peaked", 2, 32, 8192, 128,
                                            "fp16", False, k_mult=4.0, index=4),
+    # a large causal batch (K and V: 2 GiB, far beyond L2): the case the
+    # head-by-head causal order is for; not one of the target shapes
+    "b16h32n8192d128_causal": Workload("b16h32n8192d128_causal", 16, 32, 8192, 128, "bf16",
+                                       True, index=5),
 }
 
 BASE_SEED = 0
