@@ -24,16 +24,24 @@
 //
 // Tensor memory (512 columns x 128 lanes, 32-bit cells):
 //   S0 [0,128)   S1 [128,256)   O0 [256,256+D)   O1 [256+D,256+2D)
+//   d = 64 only: P0 [384,448)   P1 [448,512)
 // S_t = Q_t K_j^T (fp32).  After the softmax reads S_t it writes P_t as
-// packed 16-bit pairs over the first 64 columns of S_t, and the second MMA
-// takes P_t straight from tensor memory: S and P never leave the chip.
+// packed 16-bit pairs -- over the first 64 columns of S_t (d = 128), or in
+// P_t's own columns (d = 64) -- and the second MMA takes P_t straight from
+// tensor memory: S and P never leave the chip.
 //
 // MMA issue order per K/V block j (ping-pong between the two Q tiles, so one
-// group's softmax overlaps the other group's MMAs):
+// group's softmax overlaps the other group's MMAs), d = 128:
 //   S0_{j+1}, PV1_j, S1_{j+1}, PV0_{j+1}
 // Each S_t commit also covers the PV_t issued before it, so a softmax group
 // that sees S_t(j+1) ready may rescale O_t (PV_t(j) is complete) and the
 // MMA does not issue PV_t(j+1) until that group signals P_t ready.
+// d = 64 (P apart from S):
+//   S0_{j+1}, PV1_{j-1}, S1_{j+1}, PV0_j
+// S_t(j+1) is issued as soon as the group has loaded S_t(j) into registers
+// (an "S free" barrier), so the group finds it ready when it finishes block
+// j; each PV_t commits a "PV done" barrier that the group awaits before it
+// writes P_t again or rescales O_t.
 //
 // Every wait is bounded: after kTimeoutNs without progress the thread sets
 // the CTA's abort flag and the device status word, and all roles leave
@@ -93,15 +101,26 @@ struct Cfg {
   static constexpr int kQFull = 0, kQEmpty = 2, kKVFull = 4, kKVEmpty = 4 + kStages;
   static constexpr int kSFull = 4 + 2 * kStages, kPFull = kSFull + 2, kOFull = kPFull + 2;
   static constexpr int kDrain = kOFull + 2;
-  static constexpr int kNumBars = kDrain + 1;
+  // d = 64: P has tensor-memory columns of its own (there is room), so S_t
+  // can be overwritten as soon as the softmax has loaded it.  Two more
+  // barriers per tile: S free (kSFree + t, one arrive per warp of the
+  // tile's group) and PV done (kPVDone + t, an MMA commit after each PV).
+  static constexpr bool kSepP = (D == 64);
+  static constexpr int kSFree = kDrain + 1, kPVDone = kSFree + 2;
+  static constexpr int kNumBars = kSepP ? kPVDone + 2 : kDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag, merge flag
   // softmax row exchange: [tile][parity][half][value][row] floats, 8 KB
   static constexpr int kXchOff = (kMiscOff + 16 + 15) & ~15;
   static constexpr int kSmemBytes = kXchOff + 2 * 2 * 2 * 2 * 128 * 4 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  // tensor-memory column of S_t and O_t for Q tile t
+  // tensor-memory column of S_t, O_t and P_t for Q tile t: P_t is packed
+  // 16-bit pairs over the first 64 columns of S_t (d = 128), or in its own
+  // 64 columns after O (d = 64: S 0-255, O 256-383, P 384-511)
   static __device__ __forceinline__ uint32_t col_s(int t) { return 128u * t; }
   static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + D * t; }
+  static __device__ __forceinline__ uint32_t col_p(int t) {
+    return kSepP ? 256u + 2u * D + 64u * t : col_s(t);
+  }
   static constexpr uint32_t kIdescS = idesc_f16(BF16, false, 128, 128);
   static constexpr uint32_t kIdescO = idesc_f16(BF16, true, 128, D);
   // Five warpgroups -- four of softmax (eight warps per Q tile) and one with
@@ -292,6 +311,12 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
       mbar_init(bar(C::kOFull + t), 1);
     }
     mbar_init(bar(C::kDrain), 1);
+    if constexpr (C::kSepP) {
+      for (int t = 0; t < 2; ++t) {
+        mbar_init(bar(C::kSFree + t), 8);  // one arrive per softmax warp of the tile's group
+        mbar_init(bar(C::kPVDone + t), 1);
+      }
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -399,10 +424,11 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
         const uint64_t vd = vdesc0 + ((sbase + C::kKVOff + vslot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk) {
-          mma_ts_if(leader, tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, vd + kk * (2048 >> 4),
+          mma_ts_if(leader, tmem + C::col_o(t), tmem + C::col_p(t) + kk * 8, vd + kk * (2048 >> 4),
                  C::kIdescO, (acc || kk > 0) ? 1u : 0u);
         }
       };
+      if constexpr (!C::kSepP) {
       // The loop is rotated so that the iteration boundary (and the release
       // of a K slot) falls right after PV0's MMAs are queued: between the end
       // of S1's issue and the start of PV0's there is then only one commit
@@ -492,6 +518,84 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
             vs = nvs;
           }
         }
+      }
+      } else {
+      // d = 64, P in its own columns.  Per block j the MMAs go
+      //   S0(j+1), PV1(j-1), S1(j+1), PV0(j)
+      // (the order in which their inputs become ready).  S_t(j+1) waits only
+      // until the softmax has loaded S_t(j) into registers (S free), so each
+      // softmax group finds its next S ready when it finishes a block;
+      // PV_t(j) waits for P_t(j) and commits PV done, which the softmax
+      // awaits before it writes P_t(j+1) or rescales O_t.  An item's first S
+      // waits for the S free of the previous item's last block, so it
+      // overlaps that block and its epilogue.
+      uint32_t ring = 0;  // K/V ring entries taken by earlier items: K_j at ring + 2j, V_j next
+      uint32_t sfree_par[2] = {0, 0};
+      bool s_held[2] = {false, false};  // S_t holds an S whose S free is still to be awaited
+      auto kv_slot = [&](uint32_t idx) -> uint32_t { return idx % C::kStages; };
+      auto wait_kv = [&](uint32_t idx) {
+        return wait_bar(bar(C::kKVFull + kv_slot(idx)), (idx / C::kStages) & 1u, abort_flag,
+                        p.status);
+      };
+      // S_t(j) of a tile with n blocks: its commits, and the Q release after the last
+      auto s_mma = [&](int t, int j, int n) -> bool {
+        if (s_held[t]) {
+          if (!wait_bar(bar(C::kSFree + t), sfree_par[t], abort_flag, p.status)) return false;
+          sfree_par[t] ^= 1u;
+        }
+        if (!wait_kv(ring + 2u * j)) return false;
+        tc_fence_after();
+        issue_s(t, kv_slot(ring + 2u * j));
+        mma_commit_if(leader, bar(C::kSFull + t));
+        if (j + 1 == n) mma_commit_if(leader, bar(C::kQEmpty + t));
+        s_held[t] = true;
+        return true;
+      };
+      auto pv_mma = [&](int t, int j) -> bool {
+        if (!wait_bar(bar(C::kPFull + t), p_phase[t], abort_flag, p.status)) return false;
+        p_phase[t] ^= 1u;
+        if (!wait_kv(ring + 2u * j + 1u)) return false;
+        tc_fence_after();
+        issue_pv(t, kv_slot(ring + 2u * j + 1u), j > 0);
+        mma_commit_if(leader, bar(C::kPVDone + t));
+        return true;
+      };
+      for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_units; ++round) {
+        const int item = round_item(round, p);
+        if (item < 0) continue;
+        const Item it = decode_unit(item, p);
+        const int n0 = it.n0, n1 = it.n1;  // n1: 0 (no tile 1), n0 or n0 + 1
+        const int n_max = n0 > n1 ? n0 : n1;
+        if (!(ok = wait_bar(bar(C::kQFull + 0), q_phase[0], abort_flag, p.status))) break;
+        q_phase[0] ^= 1u;
+        if (!(ok = s_mma(0, 0, n0))) break;
+        if (n1 > 0) {
+          if (!(ok = wait_bar(bar(C::kQFull + 1), q_phase[1], abort_flag, p.status))) break;
+          q_phase[1] ^= 1u;
+          if (!(ok = s_mma(1, 0, n1))) break;
+        }
+        mma_commit_if(leader, bar(C::kKVEmpty + kv_slot(ring)));  // K_0
+        for (int j = 0; j < n_max; ++j) {
+          if (j + 1 < n0 && !(ok = s_mma(0, j + 1, n0))) break;
+          if (j >= 1 && j - 1 < n1) {
+            if (!(ok = pv_mma(1, j - 1))) break;
+            mma_commit_if(leader, bar(C::kKVEmpty + kv_slot(ring + 2u * (j - 1) + 1u)));  // V_{j-1}
+          }
+          if (j + 1 < n1 && !(ok = s_mma(1, j + 1, n1))) break;
+          if (j + 1 < n_max) mma_commit_if(leader, bar(C::kKVEmpty + kv_slot(ring + 2u * (j + 1))));  // K_{j+1}
+          if (j < n0) {
+            if (!(ok = pv_mma(0, j))) break;
+            if (j >= n1)  // V_j has no tile-1 reader
+              mma_commit_if(leader, bar(C::kKVEmpty + kv_slot(ring + 2u * j + 1u)));
+          }
+        }
+        if (!ok) break;
+        if (n1 > 0 && n1 == n_max) {  // PV1 of tile 1's last block
+          if (!(ok = pv_mma(1, n1 - 1))) break;
+          mma_commit_if(leader, bar(C::kKVEmpty + kv_slot(ring + 2u * (n1 - 1) + 1u)));
+        }
+        ring += 2u * static_cast<uint32_t>(n_max);
+      }
       }
       // Drain: all issued MMAs complete before tensor memory is freed.
       mma_commit_if(leader, bar(C::kDrain));
@@ -596,6 +700,7 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
     };
     const float sl2 = p.scale_log2;
     uint32_t s_par = 0, o_par = 0, xpar = 0;  // barrier phase bits, exchange parity
+    uint32_t pv_par = 0;                      // PV done phase bit (d = 64)
     // bar.sync cannot time out, so a warp whose wait gave up (ok == false)
     // keeps walking the same sequence of blocks, doing no work but taking
     // part in every pair barrier, so its partner can never be left waiting.
@@ -611,13 +716,19 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
       // epilogue: O / l to memory, logsumexp (one pair barrier on every
       // path, like a block)
       auto epilogue = [&]() {
-        if (ok) ok = wait_bar(bar(C::kOFull + t), o_par, abort_flag, p.status);
+        // O_t is complete after the tile's last PV (d = 64: its PV done)
+        if constexpr (C::kSepP) {
+          if (ok) ok = wait_bar(bar(C::kPVDone + t), pv_par, abort_flag, p.status);
+          pv_par ^= 1u;
+        } else {
+          if (ok) ok = wait_bar(bar(C::kOFull + t), o_par, abort_flag, p.status);
+        }
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
           pair_sync();
           return;
         }
-        o_par ^= 1u;
+        if constexpr (!C::kSepP) o_par ^= 1u;
         tc_fence_after();
         *xslot(xpar, hf, 0) = l;
         *xslot(xpar, hf, 1) = r;
@@ -705,6 +816,12 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
           tmem_ld32(tS + 64 * hf + 32, sr[1]);
           tmem_ld_wait(sr[0]);
           tmem_ld_wait(sr[1]);
+          if constexpr (C::kSepP) {
+            // S_t is in registers: the MMA may overwrite it with the next S
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kSFree + t));
+          }
           float s[64];
 #pragma unroll
           for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
@@ -743,10 +860,20 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
             alpha = ex2_approx(m - m_cand);
             m = m_cand;
           }
+          if constexpr (C::kSepP) {
+            // P_t and O_t are free once PV_t(j-1) is complete
+            if (j > 0) {
+              if (ok) ok = wait_bar(bar(C::kPVDone + t), pv_par, abort_flag, p.status);
+              pv_par ^= 1u;
+              ok = __all_sync(0xffffffffu, ok);
+              tc_fence_after();
+            }
+          }
           // P = 2^(S*scale*log2e - m), rounded to the MMA's 16-bit type, over
           // the P columns [32h, 32h + 32) of this tile (keys 64h..64h+63).
-          // Both warps have loaded their S halves (the exchange above), so the
-          // P stores cannot overwrite S the other warp still needs.
+          // Where P overlays S (d = 128), both warps have loaded their S
+          // halves (the exchange above), so the P stores cannot overwrite S
+          // the other warp still needs.
           const uint64_t sl2_2 = f2(sl2, sl2);
           const uint64_t negm_2 = f2(-m, -m);
           uint64_t sx2[2] = {0, 0};
@@ -761,7 +888,7 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
               pk[(c >> 1) & 15] = pack2<BF16>(e0, e1);
               sx2[(c >> 1) & 1] = fadd2(sx2[(c >> 1) & 1], f2(e0, e1));
             }
-            tmem_st16(tS + 32 * hf + 16 * hh, pk);
+            tmem_st16(t_lane + C::col_p(t) + 32 * hf + 16 * hh, pk);
           }
           float sum_x, sum_r;
           {
