@@ -909,7 +909,8 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
           r = r * alpha + sum_r;
           // Conditional rescale of this half of the running output (v4
           // pseudo-code panel: "if need_rescale(m, m_new): acc *= exp(m -
-          // m_new)").  PV_t(j-1) is complete: its commit precedes S_t(j)'s;
+          // m_new)").  PV_t(j-1) is complete -- its commit precedes S_t(j)'s
+          // (d = 128), or its PV done was awaited above (d = 64) -- and
           // PV_t(j) waits for this block's signal.
           if (j > 0 && __any_sync(0xffffffffu, need)) {
             const uint32_t tO = t_lane + C::col_o(t) + (D / 2) * hf;

@@ -160,7 +160,7 @@ def test_causal_row_zero_is_v0():
     assert np.max(np.abs(lse[:, :, 0] - s00) / np.maximum(1, np.abs(s00))) <= LSE_REL
 
 
-# Non-causal d = 128 shapes whose last round of work items is cut into key
+# Non-causal shapes whose last round of work items is cut into key
 # pieces (the wave-tail split): k = 4 pieces with every item split, an odd
 # tile count with a ragged end, k = 3 with one block per piece, and a mix of
 # whole and split items (k = 2) on a 152-SM device.
@@ -172,13 +172,14 @@ SPLIT_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("B,H,N,dtype", SPLIT_SHAPES,
                          ids=[f"b{b}h{h}n{n}-{str(t)[6:]}" for b, h, n, t in SPLIT_SHAPES])
-def test_parity_wave_tail_split(B, H, N, dtype):
-    q, k, v = make_qkv(B, H, N, 128, dtype, seed=60 + N + H)
+def test_parity_wave_tail_split(B, H, N, dtype, d):
+    q, k, v = make_qkv(B, H, N, d, dtype, seed=60 + N + H)
     o, lse = run_gpu(q, k, v, False)
-    o_ref, lse_ref = oracle.attn_fwd(q, k, v, False, 1.0 / math.sqrt(128))
-    assert_close(o, lse, o_ref, lse_ref, f"split {B},{H},{N},{dtype}")
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, False, 1.0 / math.sqrt(d))
+    assert_close(o, lse, o_ref, lse_ref, f"split {B},{H},{N},d={d},{dtype}")
 
 
 def _random_cases(n, seed):
@@ -211,18 +212,19 @@ def test_parity_random_shapes(B, H, N, d, causal, dtype):
     assert_close(o, lse, o_ref, lse_ref, f"{B},{H},{N},{d},causal={causal},{dtype}")
 
 
-def test_wave_tail_split_peaked_rows():
+@pytest.mark.parametrize("d", [64, 128])
+def test_wave_tail_split_peaked_rows(d):
     """Pieces of one row see very different maxima (K scaled x6, sorted so
     the largest logits sit in the last piece): the merge must weigh each
     piece by its own max and sum."""
-    B, H, N, d = 1, 3, 2048, 128
+    B, H, N = 1, 3, 2048
     q, k, v = make_qkv(B, H, N, d, torch.bfloat16, seed=61, k_mult=6.0)
     order = torch.argsort((q[0, 0].float().mean(0) @ k[0].float().transpose(-1, -2)).mean(0))
     k = k[:, :, order].contiguous()
     for thr in (0.0, 8.0):
         o, lse = run_gpu(q, k, v, False, rescale_threshold=thr)
         o_ref, lse_ref = oracle.attn_fwd(q, k, v, False, 1.0 / math.sqrt(d))
-        assert_close(o, lse, o_ref, lse_ref, f"split peaked thr={thr}")
+        assert_close(o, lse, o_ref, lse_ref, f"split peaked thr={thr} d={d}")
 
 
 def test_deterministic_bitwise():
@@ -314,18 +316,21 @@ def test_caller_buffers_and_no_write_on_error():
     assert not torch.any(o == 7.0)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("thr", [0.0, 3.0, 8.0, 12.0])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
 @pytest.mark.parametrize("dtype,k_mult", [(torch.bfloat16, 1.0), (torch.float16, 4.0),
                                           (torch.bfloat16, 6.0)], ids=["bf16", "fp16x4", "bf16x6"])
-def test_rescale_threshold_parity(thr, causal, dtype, k_mult):
+def test_rescale_threshold_parity(thr, causal, dtype, k_mult, d):
     """Every rescale threshold gives the same softmax (numerator and
     denominator share the stale max), including 0 = rescale whenever the
-    running max grows and peaked rows (K scaled up) that force rescales."""
-    q, k, v = make_qkv(2, 3, 1100, 128, dtype, seed=31, k_mult=k_mult)
+    running max grows and peaked rows (K scaled up) that force rescales.
+    Both head dims: at d=64 the rescale waits for the previous PV through
+    its own barrier (P has columns apart from S there)."""
+    q, k, v = make_qkv(2, 3, 1100, d, dtype, seed=31, k_mult=k_mult)
     o, lse = run_gpu(q, k, v, causal, rescale_threshold=thr)
-    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 1.0 / math.sqrt(128))
-    assert_close(o, lse, o_ref, lse_ref, f"thr={thr}")
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 1.0 / math.sqrt(d))
+    assert_close(o, lse, o_ref, lse_ref, f"thr={thr} d={d}")
 
 
 def test_sorted_keys_force_rescale_every_block():
