@@ -58,11 +58,21 @@ def dist_env():
     return rank, world, local
 
 
+def _code_only(text: str) -> str:
+    """The source without comments and blank lines (no string literal in
+    these files holds a comment marker)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the library's code (comments excluded): a profile taken at one
+    hash describes every source with the same hash."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "exact_attention_forward_07_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "exact_attention_forward_07_gb300", "csrc", name)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

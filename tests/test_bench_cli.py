@@ -58,3 +58,16 @@ def test_product_package_does_not_use_the_oracle():
                 continue
             text = open(os.path.join(dirpath, name), encoding="utf-8").read()
             assert not re.search(r"\boracle\b", text), os.path.join(dirpath, name)
+
+
+def test_kernel_hash_ignores_comments():
+    """bench.py ties a committed ncu summary to the library's code by a hash
+    that skips comments and blank lines, so editing a comment keeps the
+    summary's DRAM traffic in the roofline while any code change drops it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = "int a; // note\n/* block\n comment */\n\nint b;  \n"
+    assert bench._code_only(src) == "int a;\nint b;"
+    assert bench._code_only(src) == bench._code_only(src.replace("note", "other note"))
+    assert bench._code_only(src) != bench._code_only(src.replace("int b", "int c"))
+    assert re.fullmatch(r"[0-9a-f]{16}", bench.kernel_source_hash())
