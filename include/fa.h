@@ -161,7 +161,7 @@ int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *
  *
  * q, k, v are read from, and o, lse written to, host memory in the layout
  * above (page-locked memory -- cudaHostAlloc, cudaHostRegister -- for full
- * copy speed; pageable memory works, staged by the driver).  The B*H heads
+ * copy speed; pageable memory works, staged by the CUDA driver).  The B*H heads
  * are processed in `chunks` groups (0 = FA_HOST_DEFAULT_CHUNKS, at most
  * FA_HOST_MAX_CHUNKS, at most B*H): while chunk c is computed, chunk c+1 is
  * copied to the device and chunk c-1 back to the host, on three streams of
