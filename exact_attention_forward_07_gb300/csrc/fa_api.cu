@@ -167,15 +167,27 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 bool causal_head_major(int BH, int n_qtiles, int n_pairs, int G) {
   const int64_t n = static_cast<int64_t>(BH) * n_pairs;
   if (n <= G || n > (int64_t(1) << 20)) return false;
+  // load of one item of each level (level 0 = the heaviest pair)
+  std::vector<double> w(static_cast<size_t>(n_pairs));
+  for (int level = 0; level < n_pairs; ++level) {
+    const int qt1 = 2 * (n_pairs - 1 - level) + 1;
+    w[static_cast<size_t>(level)] = (qt1 < n_qtiles ? qt1 + 1 : qt1) + 1.3;
+  }
   std::vector<double> load(static_cast<size_t>(G));
   auto balance = [&](bool head_major) {
     std::fill(load.begin(), load.end(), 0.0);
-    for (int64_t i = 0; i < n; ++i) {
-      const int64_t r = i / G, off = i - r * G;
-      const int64_t b = (r & 1) ? G - 1 - off : off;
-      const int64_t level = head_major ? i % n_pairs : i / BH;
-      const int64_t qt1 = 2 * (n_pairs - 1 - level) + 1;
-      load[static_cast<size_t>(b)] += static_cast<double>(qt1 < n_qtiles ? qt1 + 1 : qt1) + 1.3;
+    int level = 0, head = 0;  // of item i, in the order simulated
+    int64_t i = 0;
+    for (int64_t r = 0; i < n; ++r) {
+      for (int off = 0; off < G && i < n; ++off, ++i) {
+        load[static_cast<size_t>((r & 1) ? G - 1 - off : off)] += w[static_cast<size_t>(level)];
+        if (head_major) {
+          if (++level == n_pairs) level = 0;
+        } else if (++head == BH) {
+          head = 0;
+          ++level;
+        }
+      }
     }
     double sum = 0.0, mx = 0.0;
     for (double x : load) {
