@@ -8,9 +8,11 @@ an absolute floor of 1e-3 where LSE is near zero).
 Small and medium shapes are compared element by element over the whole
 output; they span several 128-row tiles, ragged tails (N % 128 != 0), an
 odd number of Q tiles (the second tile of the last pair absent), N = 1 and
-both head dims and dtypes.  The full-size workloads are compared on
-sampled rows (first/last rows, tile boundaries, middle, seeded random
-rows) of a spread of heads, computed by the oracle one by one.
+both head dims and dtypes, and so is the bench's workload
+[8,16,4096,128] (both masks) at full size.  The other full-size workloads
+are compared on sampled rows (first/last rows, tile boundaries, middle,
+seeded random rows) of a spread of heads, computed by the oracle one by
+one.
 """
 import math
 
@@ -78,6 +80,18 @@ def test_parity_full_tensor(B, H, N, d, dtype, causal):
 
 @pytest.mark.parametrize("name", ["tiny_b1h1n128d64", "b4h16n1024d64", "b4h16n1024d64_causal"])
 def test_parity_small_workloads_full(name):
+    w = WORKLOADS[name]
+    q, k, v = make_workload_inputs(w)
+    o, lse = run_gpu(q, k, v, w.causal)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, w.causal, w.scale)
+    assert_close(o, lse, o_ref, lse_ref, name)
+
+
+@pytest.mark.parametrize("name", ["b8h16n4096d128", "b8h16n4096d128_causal"])
+def test_parity_bench_workload_full(name):
+    """The bench's workload, both masks, element by element over the whole
+    output: 524,288 rows of O and LSE against the oracle (about 1.1e12 fp64
+    FLOP non-causal; seconds on the host's cores)."""
     w = WORKLOADS[name]
     q, k, v = make_workload_inputs(w)
     o, lse = run_gpu(q, k, v, w.causal)
