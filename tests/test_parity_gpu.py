@@ -196,14 +196,14 @@ def test_parity_wave_tail_split(B, H, N, dtype, d):
     assert_close(o, lse, o_ref, lse_ref, f"split {B},{H},{N},d={d},{dtype}")
 
 
-def _random_cases(n, seed):
+def _random_cases(n, seed, n_lo=1, n_hi=1500, bh_hi=(4, 5)):
     rng = np.random.default_rng(seed)
     cases = []
     for _ in range(n):
         d = int(rng.choice([64, 128]))
-        N = int(rng.integers(1, 1500))
-        B = int(rng.integers(1, 4))
-        H = int(rng.integers(1, 5))
+        N = int(rng.integers(n_lo, n_hi))
+        B = int(rng.integers(1, bh_hi[0]))
+        H = int(rng.integers(1, bh_hi[1]))
         causal = bool(rng.integers(0, 2))
         dtype = torch.bfloat16 if rng.integers(0, 2) else torch.float16
         cases.append((B, H, N, d, causal, dtype))
@@ -211,6 +211,8 @@ def _random_cases(n, seed):
 
 
 RANDOM_CASES = _random_cases(32, seed=2026)
+# longer sequences (more blocks per item, more phases per barrier), fewer heads
+RANDOM_CASES += _random_cases(16, seed=2027, n_lo=1500, n_hi=6000, bh_hi=(3, 3))
 
 
 @pytest.mark.parametrize("B,H,N,d,causal,dtype", RANDOM_CASES,
@@ -413,15 +415,18 @@ def test_fa_fwd_host_pageable_fp16_and_bitwise():
     assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
-def test_parity_maximum_sequence_length(causal):
+def test_parity_maximum_sequence_length(causal, d):
     """N = FA_MAX_N (2^20), the longest sequence the boundary accepts: the
-    index arithmetic over 8192 Q tiles and 8192 K/V blocks, checked on
+    index arithmetic over 8192 Q tiles and 8192 K/V blocks (and, at d=64,
+    the S-free / PV-done barriers over that many phases), checked on
     sampled rows (first/last rows, tile boundaries, middle, random)."""
-    N, d = fa().FA_MAX_N, 128
-    q, k, v = make_qkv(1, 1, N, d, torch.bfloat16, seed=50)
+    N = fa().FA_MAX_N
+    q, k, v = make_qkv(1, 1, N, d, torch.bfloat16, seed=50 + d)
     o, lse = run_gpu(q, k, v, causal)
     rows = sample_rows(1, 1, N, n_random=8, seed=51)
     o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 1.0 / math.sqrt(d), rows=rows)
-    assert_close(o.reshape(N, d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, f"N=2^20 causal={causal}")
+    assert_close(o.reshape(N, d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref,
+                 f"N=2^20 d={d} causal={causal}")
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
