@@ -10,7 +10,11 @@ N(0,1) inputs.  Prints one JSON line (rank 0).  The metric is TFLOPS with
 
 Timing: W warm-up steps, then exactly K steps between a barrier and a
 device synchronisation on both sides, timed with CUDA events on the stream
-the kernel is launched on; the maximum over ranks is reported.  Q+K+V
+the kernel is launched on; the maximum over ranks is reported.  Without
+--steps, K is set from the warm-up timing so the timed region lasts about
+2 s (50 to 20000 steps; the largest K over ranks), which gives the 200 ms
+nvidia-smi clock samples, kept only from inside the timed region, about ten
+readings.  Q+K+V
 (384 MiB for the default) exceed the 126 MB L2, so no flush is needed
 between steps.  Under torchrun each rank runs the same workload on its own
 GPU (heads are independent: weak scaling, no data-path collective).
@@ -28,6 +32,7 @@ sample of the same workload (128 query rows of one head).
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -48,6 +53,7 @@ METRIC = "attention fwd TFLOPS (bf16, 1×GB300) and fraction of dense tensor-cor
 DEFAULT_WORKLOAD = "b8h16n4096d128"
 FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCES = ["fa_api.cu", "fa_kernel.cuh", "ptx.cuh"]
+AUTO_TIMED_S = 2.0  # timed work with no --steps: long enough for 200 ms clock samples
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "fa_fwd_kernel_b8h16n4096d128.md")
 
 
@@ -101,9 +107,11 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while running."""
+    """nvidia-smi clock/throttle samples every 200 ms while running; stop()
+    keeps the samples whose timestamps fall inside a given window (the timed
+    region), so idle time around it does not count."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -122,7 +130,8 @@ class ClockSampler:
         except OSError:
             self.proc = None
 
-    def stop(self):
+    def stop(self, window=None):
+        """window: (start, end) host times (time.time()) to keep samples from."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -131,13 +140,25 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        rows = []
+        rows, inside = [], []
         with open(self.out_path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+                if len(parts) < 10:
+                    continue
+                rows.append(parts[1:])
+                if window is not None:
+                    try:
+                        t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    except ValueError:
+                        continue
+                    if window[0] <= t <= window[1]:
+                        inside.append(parts[1:])
         os.unlink(self.out_path)
+        # the samples taken inside the window, or all of them if none were
+        scope = "timed region" if inside or window is None else "whole run (none inside the timed region)"
+        if inside:
+            rows = inside
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
 
@@ -156,7 +177,7 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(busy) if busy else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
-                "samples": len(rows), "reasons": reasons}
+                "samples": len(rows), "sampled": scope, "reasons": reasons}
 
 
 L2_BYTES = 126 * 1024 * 1024
@@ -301,9 +322,18 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
     flops = w.flops()
 
-    for _ in range(args.warmup):
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup):
+        if i == 1:
+            w0.record(stream)
         call(q, k, v, o, lse, causal=w.causal, stream=stream)
+    w1.record(stream)
     torch.cuda.synchronize(dev)
+    if args.steps is None:
+        # about 2 s of timed work, so the 200 ms clock samples cover it
+        t_step = w0.elapsed_time(w1) / (args.warmup - 1) * 1e-3
+        steps = int(min(20000, max(50, math.ceil(AUTO_TIMED_S / max(t_step, 1e-7)))))
+        args.steps = int(max_over_ranks(float(steps), world))
     status = fa.fa_get_status(stream)
     if status != 0:
         raise RuntimeError(f"kernel status {status}: {fa.fa_strerror(status)}")
@@ -316,14 +346,16 @@ def run_ours(args, w):
     torch.cuda.synchronize(dev)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    t_begin = time.time()
     ev0.record(stream)
     for _ in range(args.steps):
         call(q, k, v, o, lse, causal=w.causal, stream=stream)
     ev1.record(stream)
     torch.cuda.synchronize(dev)
+    t_end = time.time()
     barrier(world)
     # ------------------------------------------------------------------------
-    clocks = sampler.stop()
+    clocks = sampler.stop(window=(t_begin, t_end))
     ms_local = ev0.elapsed_time(ev1)
     value, ms_total = job_throughput(flops, args.steps, ms_local, world)
     ms_step = ms_total / args.steps
@@ -412,7 +444,9 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__,
                                  formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: about 2 s of work for our arm, 500 for the "
+                         "reference arm)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
@@ -431,6 +465,8 @@ def main(argv=None):
                   file=sys.stderr)
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
+        if args.steps is None:
+            args.steps = 500
         return run_reference(args, w)
     return run_ours(args, w)
 
