@@ -428,6 +428,8 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
                  C::kIdescO, (acc || kk > 0) ? 1u : 0u);
         }
       };
+      // Two issue loops, kept flat: d = 128 (P over S) here, d = 64 (P in its
+      // own columns) in the else branch below.
       if constexpr (!C::kSepP) {
       // The loop is rotated so that the iteration boundary (and the release
       // of a K slot) falls right after PV0's MMAs are queued: between the end
@@ -519,7 +521,7 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
           }
         }
       }
-      } else {
+      } else {  // d = 64
       // d = 64, P in its own columns.  Per block j the MMAs go
       //   S0(j+1), PV1(j-1), S1(j+1), PV0(j)
       // (the order in which their inputs become ready).  S_t(j+1) waits only
