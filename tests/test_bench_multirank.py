@@ -25,7 +25,10 @@ def _worker(rank, world, port, out):
         bench.barrier(world)
         ms_local = 100.0 if rank == 0 else 250.0
         tflops, ms_max = bench.job_throughput(1e12, 10, ms_local, world)
-        out[rank] = (tflops, ms_max, bench.dist_env())
+        # without --steps each rank sizes its run from its own warm-up; all
+        # ranks then time the largest of those step counts
+        steps = int(bench.max_over_ranks(float(2900 if rank == 0 else 3100), world))
+        out[rank] = (tflops, ms_max, bench.dist_env(), steps)
         bench.barrier(world)
     finally:
         dist.destroy_process_group()
@@ -39,7 +42,8 @@ def test_two_rank_gloo_aggregation():
         mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
     for rank in range(world):
-        tflops, ms_max, env = res[rank]
+        tflops, ms_max, env, steps = res[rank]
+        assert steps == 3100                        # every rank times the same K
         assert ms_max == 250.0                      # slowest rank
         assert tflops == pytest.approx(2 * 1e12 * 10 / 0.25 / 1e12)  # 80 TFLOPS
         assert env == (rank, world, rank)
