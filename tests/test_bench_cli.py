@@ -71,3 +71,46 @@ def test_kernel_hash_ignores_comments():
     assert bench._code_only(src) == bench._code_only(src.replace("note", "other note"))
     assert bench._code_only(src) != bench._code_only(src.replace("int b", "int c"))
     assert re.fullmatch(r"[0-9a-f]{16}", bench.kernel_source_hash())
+
+
+def test_clock_samples_kept_only_inside_the_timed_region(tmp_path):
+    """The clock record of a bench line uses only the nvidia-smi samples whose
+    timestamps fall inside the timed region, and says so when none did."""
+    sys.path.insert(0, ROOT)
+    import datetime
+    import bench
+
+    class _Done:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    def sampler_with(lines):
+        s = bench.ClockSampler(0)
+        s.out_path = str(tmp_path / "clocks.csv")
+        with open(s.out_path, "w") as f:
+            f.write("".join(lines))
+        s.fh = open(s.out_path, "a")
+        s.proc = _Done()
+        return s
+
+    t0 = datetime.datetime(2026, 1, 2, 3, 4, 5)
+    def row(dt_s, mhz, watts, power_cap):
+        ts = (t0 + datetime.timedelta(seconds=dt_s)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        cap = "Active" if power_cap else "Not Active"
+        return f"{ts}, 0, {mhz}, 2070, {watts}, 0x4, Not Active, Not Active, Not Active, {cap}\n"
+
+    lines = [row(0.0, 2070, 120, False), row(1.0, 1800, 1390, True), row(1.2, 1820, 1388, True),
+             row(1.4, 1790, 1391, True), row(3.0, 2070, 150, False)]
+    window = ((t0 + datetime.timedelta(seconds=0.9)).timestamp(),
+              (t0 + datetime.timedelta(seconds=1.5)).timestamp())
+    rec = sampler_with(lines).stop(window=window)
+    assert rec["samples"] == 3 and rec["sampled"] == "timed region"
+    assert rec["sm_mhz"] == 1800 and rec["power_w_max"] == 1391
+    assert rec["reasons"] == ["sw_power_cap"]
+    # a window that no sample falls in: the whole run, marked as such
+    far = (window[0] + 100, window[1] + 100)
+    rec = sampler_with(lines).stop(window=far)
+    assert rec["samples"] == 5 and rec["sampled"].startswith("whole run")
