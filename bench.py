@@ -4,18 +4,22 @@
                     [--workload NAME]
 
 A step is one forward (O and LSE) over the whole workload; by default the
-bf16 d=128, N=4096 batch [B=8, H=16, N=4096, d=128], non-causal, seeded
-N(0,1) inputs.  Prints one JSON line (rank 0).  The metric is TFLOPS with
-4*B*H*N^2*d FLOPs per step (halved when causal).
+largest bf16 shape of the target set, the long causal sequence
+[B=1, H=32, N=16384, d=128] with seeded N(0,1) inputs.  Prints one JSON
+line (rank 0).  The metric is TFLOPS with 4*B*H*N^2*d FLOPs per step
+(halved when causal).
 
 Timing: W warm-up steps, then exactly K steps between a barrier and a
 device synchronisation on both sides, timed with CUDA events on the stream
 the kernel is launched on; the maximum over ranks is reported.  Without
 --steps, K is set from the warm-up timing so the timed region lasts about
-2 s (50 to 20000 steps; the largest K over ranks), which gives the 200 ms
-nvidia-smi clock samples, kept only from inside the timed region, about ten
-readings.  Q+K+V
-(384 MiB for the default) exceed the 126 MB L2, so no flush is needed
+2 s (50 to 20000 steps; the largest K over ranks).  SM clock, power and
+clock-event reasons are read from NVML every 2 ms on a background thread
+and only the samples taken inside the timed region are kept (about ten in a
+20-step run of the default workload).  The roofline's peak is the measured
+burst bf16 rate for a timed region under a second and the sustained one
+for longer runs (the board reaches its power limit within about a second).
+Q+K+V (384 MiB for the default) exceed the 126 MB L2, so no flush is needed
 between steps.  Under torchrun each rank runs the same workload on its own
 GPU (heads are independent: weak scaling, no data-path collective).
 
@@ -32,14 +36,12 @@ sample of the same workload (128 query rows of one head).
 from __future__ import annotations
 
 import argparse
-import datetime
 import hashlib
 import json
 import math
 import os
 import re
 import statistics
-import subprocess
 import sys
 import time
 
@@ -50,11 +52,17 @@ if ROOT not in sys.path:
 from attn_inputs import WORKLOADS, make_workload_inputs  # noqa: E402
 
 METRIC = "attention fwd TFLOPS (bf16, 1×GB300) and fraction of dense tensor-core peak"
-DEFAULT_WORKLOAD = "b8h16n4096d128"
+DEFAULT_WORKLOAD = "b1h32n16384d128_causal"
 FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCES = ["fa_api.cu", "fa_kernel.cuh", "ptx.cuh"]
-AUTO_TIMED_S = 2.0  # timed work with no --steps: long enough for 200 ms clock samples
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "fa_fwd_kernel_b8h16n4096d128.md")
+AUTO_TIMED_S = 2.0  # timed work with no --steps
+SUSTAINED_AFTER_S = 1.0  # timed regions at least this long compare against the sustained peak
+CPU_SAMPLE_FLOP = 1.1e12  # oracle work of the default cpu_baseline sample (~17 s on 16 cores)
+
+
+def profile_summary(workload: str) -> str:
+    """The committed ncu summary of the kernel on a workload."""
+    return os.path.join(ROOT, "profiles", f"fa_fwd_kernel_{workload}.md")
 
 
 def dist_env():
@@ -82,11 +90,12 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, or None when
-    the kernel sources changed since that capture."""
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary of `workload`,
+    or None when there is none or the kernel sources changed since that
+    capture."""
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(profile_summary(workload)).read()
     except OSError:
         return None
     m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
@@ -96,88 +105,136 @@ def profiled_traffic():
     return float(m_traffic.group(1))
 
 
-def measured_peaks():
+def measured_peaks(sustained: bool = False):
+    """(bf16 TFLOP/s, description): the measured burst or sustained
+    cuBLAS rate, else the fallback figure."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["bf16_tflops"]), "measured"
+        return float(d[key]), f"{key}, measured"
     except (OSError, KeyError, ValueError):
-        return FALLBACK_BF16_TFLOPS, "fallback"
+        return (1700.0 if sustained else FALLBACK_BF16_TFLOPS), f"{key}, fallback"
+
+
+# NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*)
+_NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+class NvmlReader:
+    """Read-only NVML queries through ctypes (libnvidia-ml ships with the
+    driver; no Python package needed): SM clock, its maximum, board power
+    and the active clock-event reasons of one GPU.  Nothing is set."""
+
+    def __init__(self, pci_bus_id=None, index=0):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        rc = 1
+        if pci_bus_id:
+            rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(),
+                                                           ctypes.byref(self.h))
+        if rc != 0:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h))
+        if rc != 0:
+            raise OSError("no NVML handle for the GPU")
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.max_mhz = self._uint(self.lib.nvmlDeviceGetMaxClockInfo, 1)
+
+    def _uint(self, fn, *args):
+        v = self.ct.c_uint(0)
+        return float(v.value) if fn(self.h, *args, self.ct.byref(v)) == 0 else None
+
+    def __call__(self):
+        """(sm_mhz, sm_max_mhz, power_w, reason bits)"""
+        sm = self._uint(self.lib.nvmlDeviceGetClockInfo, 1)  # NVML_CLOCK_SM
+        mw = self._uint(self.lib.nvmlDeviceGetPowerUsage)
+        bits = self.ct.c_ulonglong(0)
+        ok = self.reasons_fn(self.h, self.ct.byref(bits)) == 0
+        return sm, self.max_mhz, (mw / 1000.0 if mw is not None else None), (
+            bits.value if ok else None)
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while running; stop()
-    keeps the samples whose timestamps fall inside a given window (the timed
-    region), so idle time around it does not count."""
+    """SM clock, power and clock-event reasons sampled every `period_s`
+    (2 ms by default, read-only NVML) on a background thread while the
+    benchmark runs; stop() keeps the samples whose host timestamps fall
+    inside a given window (the timed region), so idle time around it does
+    not count.  A 20-step timed region of a millisecond kernel then still
+    holds about ten samples."""
 
-    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    def __init__(self, reader, period_s=0.002):
+        self.reader = reader
+        self.period_s = period_s
+        self.samples = []  # (host time, sm_mhz, sm_max_mhz, power_w, reason bits)
+        self._stop = None
+        self._thread = None
 
-    def __init__(self, gpu_index: int):
-        self.gpu_index = gpu_index
-        self.proc = None
-        self.out_path = os.path.join("/tmp", f"fa_clocks_{os.getpid()}.csv")
+    @classmethod
+    def for_device(cls, dev_index: int):
+        import torch
+        props = torch.cuda.get_device_properties(dev_index)
+        bus = None
+        if hasattr(props, "pci_bus_id"):
+            bus = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                         getattr(props, "pci_device_id", 0))
+        try:
+            return cls(NvmlReader(bus, dev_index))
+        except (OSError, AttributeError):
+            return cls(None)
 
     def start(self):
-        try:
-            self.fh = open(self.out_path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=self.fh, stderr=subprocess.DEVNULL)
-        except OSError:
-            self.proc = None
+        import threading
+        if self.reader is None:
+            return
+        self._stop = threading.Event()
+
+        def loop():
+            while not self._stop.is_set():
+                t = time.time()
+                try:
+                    self.samples.append((t, *self.reader()))
+                except Exception:  # a failed read only loses that sample
+                    pass
+                self._stop.wait(self.period_s)
+
+        self._thread = threading.Thread(target=loop, daemon=True)
+        self._thread.start()
 
     def stop(self, window=None):
         """window: (start, end) host times (time.time()) to keep samples from."""
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.fh.close()
-        rows, inside = [], []
-        with open(self.out_path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 10:
-                    continue
-                rows.append(parts[1:])
-                if window is not None:
-                    try:
-                        t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                    except ValueError:
-                        continue
-                    if window[0] <= t <= window[1]:
-                        inside.append(parts[1:])
-        os.unlink(self.out_path)
-        # the samples taken inside the window, or all of them if none were
-        scope = "timed region" if inside or window is None else "whole run (none inside the timed region)"
+        if self.reader is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["NVML unavailable"],
+                    "source": None}
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+        rows = self.samples
+        inside = [r for r in rows if window is None or window[0] <= r[0] <= window[1]]
+        scope = "timed region" if inside or window is None else \
+            "whole run (none inside the timed region)"
         if inside:
             rows = inside
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
-                return None
-        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
-        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
-        power = [num(r[3]) for r in rows if num(r[3]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4)
-                          if r[5 + i].lower().startswith("active")})
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"],
+                    "source": "nvml"}
+        sm = [r[1] for r in rows if r[1] is not None]
+        smax = [r[2] for r in rows if r[2] is not None]
+        power = [r[3] for r in rows if r[3] is not None]
+        reasons = sorted({name for r in rows if r[4] is not None
+                          for bit, name in _NVML_REASONS.items() if r[4] & bit})
         busy = [s for s in sm if smax and s >= 0.3 * max(smax)] or sm
         return {"sm_mhz": statistics.median(busy) if busy else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
-                "samples": len(rows), "sampled": scope, "reasons": reasons}
+                "samples": len(rows), "sampled": scope, "reasons": reasons,
+                "source": f"nvml every {self.period_s * 1e3:g} ms"}
 
 
 L2_BYTES = 126 * 1024 * 1024
@@ -330,7 +387,7 @@ def run_ours(args, w):
     w1.record(stream)
     torch.cuda.synchronize(dev)
     if args.steps is None:
-        # about 2 s of timed work, so the 200 ms clock samples cover it
+        # about 2 s of timed work
         t_step = w0.elapsed_time(w1) / (args.warmup - 1) * 1e-3
         steps = int(min(20000, max(50, math.ceil(AUTO_TIMED_S / max(t_step, 1e-7)))))
         args.steps = int(max_over_ranks(float(steps), world))
@@ -338,9 +395,9 @@ def run_ours(args, w):
     if status != 0:
         raise RuntimeError(f"kernel status {status}: {fa.fa_strerror(status)}")
 
-    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler = ClockSampler.for_device(dev.index if dev.index is not None else 0)
     sampler.start()
-    time.sleep(0.25)
+    time.sleep(0.05)
     # ---------------------------------------------------------- timed region
     barrier(world)
     torch.cuda.synchronize(dev)
@@ -405,17 +462,28 @@ def run_ours(args, w):
             dist.destroy_process_group()
         return 0
 
-    peak, peak_kind = measured_peaks()
+    # The time and the clock it ran at: milliseconds x median MHz per step
+    # (thousands of SM cycles) and the FLOP each SM did per cycle.
+    if clocks.get("sm_mhz"):
+        n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        clocks["ms_per_step_x_mhz"] = ms_local / args.steps * clocks["sm_mhz"]
+        clocks["flop_per_clock_per_sm"] = flops / (
+            ms_local / args.steps * 1e-3 * clocks["sm_mhz"] * 1e6 * n_sm)
+    sustained = ms_local * 1e-3 >= SUSTAINED_AFTER_S
+    peak, peak_kind = measured_peaks(sustained)
     roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peak,
                 "unit": "TFLOP/s", "frac": kernel_tflops / peak,
-                "peak_source": f"bf16_tflops burst, {peak_kind}",
-                "traffic": profiled_traffic(),
+                "peak_source": peak_kind + (" (timed region >= 1 s)" if sustained else
+                                            " (timed region < 1 s)"),
+                "traffic": profiled_traffic(w.name),
                 "kernel": "fa_fwd_kernel<%d,%s>" % (w.d, "bf16" if w.dtype == "bf16" else "fp16")}
 
     cpu = None
     if not args.no_cpu_baseline:
         q64 = [q_h, k_h, v_h]
-        n_heads = max(1, int(args.cpu_heads))
+        n_heads = int(args.cpu_heads)
+        if n_heads <= 0:  # about CPU_SAMPLE_FLOP of oracle work: whole heads
+            n_heads = max(1, round(CPU_SAMPLE_FLOP / (flops / (w.B * w.H))))
         tf, dt, desc = oracle_sample(w, *q64, n_heads=n_heads)
         cpu = {"value": tf, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
                "sample": desc, "seconds": dt}
@@ -452,7 +520,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--e2e-chunks", type=int, default=8)
-    ap.add_argument("--cpu-heads", type=int, default=128)
+    ap.add_argument("--cpu-heads", type=int, default=0,
+                    help="heads in the cpu_baseline sample (0: about 1.1e12 FLOP of them)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

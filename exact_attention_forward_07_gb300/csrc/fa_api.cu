@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 #include <vector>
 
 #include "fa.h"
@@ -24,10 +25,16 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
   std::once_flag once;
   int err = FA_OK;  // FA_ERR_DEVICE / FA_ERR_CUDA if the device is unusable
+  int dev = 0;
   int sm_count = 0;
   unsigned *status = nullptr;  // device address of g_fa_status
+  std::once_flag pool_once;
   cudaMemPool_t pool = nullptr;  // stream-ordered scratch for split items (none: no split)
   uint8_t *noalloc = nullptr;    // device address of g_fa_noalloc_scratch
+  // causal item order chosen per (B*H, Q tiles): the host simulation runs
+  // once per shape
+  std::mutex order_mu;
+  std::unordered_map<uint64_t, bool> order_cache;
   // fa_fwd_host: copy-in, compute and copy-out streams, events and device
   // staging memory (created on first use, staging grown as needed); calls
   // on one device take host_mu, so they run one at a time
@@ -69,8 +76,27 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Bytes of the wave-tail split's scratch for `pieces` pieces of `items`
+// items at head dim D: partial O (256 rows x D fp32 per piece), row
+// statistics (3 x 256 fp32 per piece, rounded up to 256 bytes) and one
+// counter per item.  Parts: [0] O, [1] statistics, [2] counters.
+void split_scratch_bytes(size_t pieces, size_t items, int D, size_t part[3]) {
+  part[0] = pieces * 256 * static_cast<size_t>(D) * sizeof(float);
+  part[1] = (pieces * 256 * 3 * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  part[2] = items * sizeof(unsigned);
+}
+
+// The most any split plan needs on a device with G SMs: at most one piece
+// per SM (R items x k pieces with k <= G / R) at the larger head dim.
+size_t split_scratch_max(int G) {
+  size_t part[3];
+  split_scratch_bytes(static_cast<size_t>(G), static_cast<size_t>(G), 128, part);
+  return part[0] + part[1] + part[2];
+}
+
 // Device checks once per device: compute capability 10.3 (the kernels are
-// built for sm_103a only), SM count, address of the status word.
+// built for sm_103a only), SM count, device addresses of the status word
+// and of fa_fwd_noalloc's fixed array.  Allocates no device memory.
 int device_state(DeviceState **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -98,6 +124,7 @@ int device_state(DeviceState **out) {
       s.err = FA_ERR_CUDA;
       return;
     }
+    s.dev = dev;
     s.status = static_cast<unsigned *>(addr);
     void *scr = nullptr;
     cudaError_t e5 = cudaGetSymbolAddress(&scr, g_fa_noalloc_scratch);
@@ -107,26 +134,44 @@ int device_state(DeviceState **out) {
       return;
     }
     s.noalloc = static_cast<uint8_t *>(scr);
-    // A private memory pool that keeps what it has allocated, so the split
-    // schedule's scratch memory costs no device allocation after the first
-    // call.  Without it the library runs every item whole.
+  });
+  if (s.err != FA_OK) return s.err;
+  *out = &s;
+  return FA_OK;
+}
+
+// The split-scratch pool of the device, created by the first call of an
+// entry point that may use it (never by fa_fwd_noalloc): a private memory
+// pool that keeps what it has allocated, filled at once with the largest
+// scratch any call can need (taken and given back on a private stream), so
+// that later calls issued one stream at a time make no device allocation.
+// Without a pool the library runs every item whole; a failed reservation
+// only leaves the pool to grow on first use.
+void ensure_pool(DeviceState &s, int dev) {
+  std::call_once(s.pool_once, [&] {
     cudaMemPoolProps props;
     std::memset(&props, 0, sizeof(props));
     props.allocType = cudaMemAllocationTypePinned;
     props.handleTypes = cudaMemHandleTypeNone;
     props.location.type = cudaMemLocationTypeDevice;
     props.location.id = dev;
-    if (cudaMemPoolCreate(&s.pool, &props) == cudaSuccess) {
-      uint64_t keep = UINT64_MAX;
-      cudaMemPoolSetAttribute(s.pool, cudaMemPoolAttrReleaseThreshold, &keep);
-    } else {
+    if (cudaMemPoolCreate(&s.pool, &props) != cudaSuccess) {
       s.pool = nullptr;
       cudaGetLastError();
+      return;
     }
+    uint64_t keep = UINT64_MAX;
+    cudaMemPoolSetAttribute(s.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    cudaStream_t st = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess) {
+      void *r = nullptr;
+      if (cudaMallocFromPoolAsync(&r, split_scratch_max(s.sm_count), s.pool, st) == cudaSuccess)
+        cudaFreeAsync(r, st);
+      cudaStreamSynchronize(st);
+      cudaStreamDestroy(st);
+    }
+    cudaGetLastError();
   });
-  if (s.err != FA_OK) return s.err;
-  *out = &s;
-  return FA_OK;
 }
 
 // [B*H, N, d] view, box 128 rows x 64 columns, 128-byte swizzle; rows past
@@ -232,10 +277,19 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
   p.causal = causal ? 1 : 0;
   // K and V of all heads beyond 64 MiB: L2 (126 MB) no longer holds them
   const double kv_bytes = 2.0 * static_cast<double>(BH) * static_cast<double>(N) * D * 2.0;
-  p.causal_head_major = causal && kv_bytes > 64.0 * 1024 * 1024 &&
-                                causal_head_major(p.BH, p.n_qtiles, p.n_pairs, ds.sm_count)
-                            ? 1
-                            : 0;
+  p.causal_head_major = 0;
+  if (causal && kv_bytes > 64.0 * 1024 * 1024) {
+    const uint64_t key = (static_cast<uint64_t>(p.BH) << 32) | static_cast<uint32_t>(p.n_qtiles);
+    std::lock_guard<std::mutex> lock(ds.order_mu);
+    auto hit = ds.order_cache.find(key);
+    if (hit == ds.order_cache.end()) {
+      if (ds.order_cache.size() >= 4096) ds.order_cache.clear();  // bounded
+      hit = ds.order_cache
+                .emplace(key, causal_head_major(p.BH, p.n_qtiles, p.n_pairs, ds.sm_count))
+                .first;
+    }
+    p.causal_head_major = hit->second ? 1 : 0;
+  }
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.rescale_thr = thr;
 
@@ -261,10 +315,9 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
     if (k > fa::kMaxSplit) k = fa::kMaxSplit;
     if (k > p.n_qtiles) k = p.n_qtiles;
     if (k >= 2) {
-      const size_t pieces = static_cast<size_t>(R) * k;
-      const size_t bytes_o = pieces * 256 * D * sizeof(float);
-      const size_t bytes_st = (pieces * 256 * 3 * sizeof(float) + 255) & ~static_cast<size_t>(255);
-      const size_t bytes_cnt = static_cast<size_t>(R) * sizeof(unsigned);
+      size_t part[3];
+      split_scratch_bytes(static_cast<size_t>(R) * k, static_cast<size_t>(R), D, part);
+      const size_t bytes_o = part[0], bytes_st = part[1], bytes_cnt = part[2];
       const size_t need = bytes_o + bytes_st + bytes_cnt;
       uint8_t *base = nullptr;
       // Under stream capture the scratch becomes a graph allocation
@@ -347,6 +400,7 @@ int fwd_common(bool bf16, const void *q, const void *k, const void *v, void *o, 
   DeviceState *ds = nullptr;
   int rc = device_state(&ds);
   if (rc != FA_OK) return rc;
+  if (!noalloc) ensure_pool(*ds, ds->dev);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 #define FA_LAUNCH(DD, BB, SLOT) \
   launch<DD, BB>(*ds, SLOT, q, k, v, o, lse, BH, N, causal, scale, thr, noalloc, st)

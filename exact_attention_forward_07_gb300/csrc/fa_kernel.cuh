@@ -223,11 +223,17 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 }
 
 // Drain wait: bounded by time only (the awaited copy or MMA needs nothing
-// from other threads to finish).
-__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+// from other threads to finish).  Giving up is reported like any other
+// timeout, so the caller learns that memory may still have been in use.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                           unsigned *status) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kTimeoutNs) return;
+    if (globaltimer_ns() - t0 > kTimeoutNs) {
+      *abort_flag = 1;
+      atomicOr(status, kStatusTimeout);
+      return;
+    }
   }
 }
 
@@ -386,11 +392,11 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
       for (int s = 0; s < C::kStages; ++s) {
         if (static_cast<uint32_t>(s) < kv_loads) {
           const uint32_t cnt = (kv_loads - s + C::kStages - 1) / C::kStages;
-          wait_drain(bar(C::kKVFull + s), (cnt - 1) & 1u);
+          wait_drain(bar(C::kKVFull + s), (cnt - 1) & 1u, abort_flag, p.status);
         }
       }
       for (int t = 0; t < 2; ++t)
-        if (q_loads[t]) wait_drain(bar(C::kQFull + t), (q_loads[t] - 1) & 1u);
+        if (q_loads[t]) wait_drain(bar(C::kQFull + t), (q_loads[t] - 1) & 1u, abort_flag, p.status);
     }
     } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------- MMA issue
@@ -601,7 +607,7 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
       }
       // Drain: all issued MMAs complete before tensor memory is freed.
       mma_commit_if(leader, bar(C::kDrain));
-      wait_drain(bar(C::kDrain), 0);
+      wait_drain(bar(C::kDrain), 0, abort_flag, p.status);
     }
     }
   } else {
@@ -952,6 +958,10 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
           if (ok)
             last = atomicAdd(p.part_cnt + it.piece / p.split_k, 1u) ==
                    static_cast<unsigned>(p.split_k - 1);
+          // acquire side of the count: the other pieces' scratch writes
+          // (each fenced before its own count) are ordered before the
+          // merge's reads
+          if (last) __threadfence();
           *merge_flag = last;
         }
         softmax_sync();

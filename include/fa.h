@@ -22,22 +22,26 @@
  * Ownership: the caller allocates and owns q, k, v, o and lse.  Non-causal
  * calls whose last round of work items is split along the keys (the
  * wave-tail split: when fewer than half the SMs would have an item in the
- * last round) take scratch memory for the pieces' partial results -- at
+ * last round) need scratch memory for the pieces' partial results -- at
  * most one piece per SM, 1 KiB * d + 3 KiB each, plus 4 bytes per split
- * item -- from
- * a stream-ordered memory pool the library creates per device; it is
- * returned to the pool behind the kernel on the same stream, and the pool
- * keeps its memory, so after the first such call no device allocation
- * happens.  If the pool cannot supply it the call runs unsplit.  Per-device
- * state (SM count, kernel attributes, one 4-byte status word, the pool) is
- * created on first use and lives until process exit.  o and lse must not
- * overlap q, k, v or each other.
+ * item; about 20 MB on 152 SMs.  It comes from a stream-ordered memory pool
+ * that the library creates per device when it first sets the device up,
+ * and that it fills there and then with the largest amount any call can
+ * need.  A call takes its scratch from the pool and gives it back behind
+ * the kernel on the same stream; the pool keeps its memory.  So after
+ * set-up, calls issued one stream at a time allocate no device memory.
+ * Split calls running at the same time on several streams each take their
+ * own scratch, and the pool grows (once) to the most that ran at the same
+ * time.  If the pool cannot supply it the call runs unsplit.  Per-device
+ * state (SM count, kernel attributes, one 4-byte status word, the pool, the
+ * causal item order per shape) is created on first use and lives until
+ * process exit.  o and lse must not overlap q, k, v or each other.
  *
  * Execution: asynchronous on `stream` (0 = legacy default stream); no host
  * synchronisation.  Safe to call from several host threads.  fa_fwd,
- * fa_fwd_fp16, fa_fwd_ex and fa_fwd_noalloc may be captured into a CUDA
- * graph (stream capture): the split schedule's scratch then becomes a graph
- * allocation (cudaMallocAsync / cudaFreeAsync nodes) instead of pool memory.
+ * fa_fwd_fp16 and fa_fwd_ex may be captured into a CUDA graph (stream
+ * capture): the split schedule's scratch then becomes a graph allocation
+ * (cudaMallocAsync / cudaFreeAsync nodes) instead of pool memory.
  *
  * Errors: 0 on success, a negative FA_ERR_* code otherwise.  On an argument
  * error nothing is launched and o/lse are not written.  Faults seen while
@@ -129,24 +133,38 @@ int fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, 
 /*
  * fa_fwd_noalloc -- fa_fwd_ex that never allocates device memory.
  *
- * The pages have no counterpart to this entry point: it is a deployment
- * variant of this library for callers that must not allocate device memory
- * during a call.  The wave-tail split's scratch (see Ownership above) comes
- * from one fixed array of FA_NOALLOC_SCRATCH_BYTES in the library's device
- * memory, located once per device (cudaGetSymbolAddress) when the library
- * first sets the device up, instead of from the memory pool.  A call whose
- * split needs more than that -- 1024 * d + 3072 bytes per piece plus 4 per
- * split item, so at most 125 pieces at d = 128; e.g. the 144 pieces of a
- * non-causal [8,16,4096,128] call on 152 SMs -- is rejected with
- * FA_ERR_SCRATCH before anything is launched (o and lse are not written);
- * fa_fwd_ex serves it.
- * Calls that need no scratch (causal, or a last round that is not
- * split) are always accepted, and the rest give bitwise fa_fwd_ex's result.
+ * The pages have no counterpart to this entry point.  It serves callers that
+ * cannot call cudaMalloc or take memory from a pool while they run: an
+ * inference server that reserves all device memory for its own caching
+ * allocator at start-up (so a driver allocation would fail or steal from
+ * that reservation), a real-time loop that must not hit the allocator's
+ * locks and implicit synchronisation, or code that runs inside another
+ * library's allocation-free contract.  For them the wave-tail split's
+ * scratch (see Ownership above) is one fixed array of
+ * FA_NOALLOC_SCRATCH_BYTES (16 MiB) in the library's own device memory: it
+ * exists from the moment the library's device code is loaded, on every GPU
+ * that loads it, until the process exits.  Host code cannot use the array's
+ * name as a device address, so the first call on a device looks the
+ * address up once (cudaGetSymbolAddress) with that device current; make
+ * that first call before any stream capture.  Neither that set-up nor any
+ * later call allocates device memory or calls an allocating routine; the
+ * split-scratch pool of the other entry points is never created by this
+ * one.
  *
- * The array is shared by every fa_fwd_noalloc call on the device, so these
- * calls must not run concurrently: issue them on one stream, or order them
- * with events.  Arguments, layout, ownership of q/k/v/o/lse and the other
- * errors are fa_fwd_ex's.
+ * Limit: a split needs 1024 * d + 3072 bytes per piece plus 4 per split
+ * item, so at most 125 pieces fit at d = 128.  A call whose split needs more
+ * (e.g. the 144 pieces of a non-causal [8,16,4096,128] call on 152 SMs) is
+ * rejected with FA_ERR_SCRATCH before anything is launched; o and lse are
+ * not written, and fa_fwd_ex serves the same call.  Calls that need no
+ * scratch (causal, or a last round that is not split) are always accepted.
+ * Results are bitwise those of fa_fwd_ex.
+ *
+ * Every call on a device shares the one array, which keeps what the last
+ * call left in it; each call clears the piece counters it uses before its
+ * kernel runs.  Calls that overlap on the GPU race on the array and give
+ * undefined results: issue them on one stream, or order them with events.
+ * Arguments, layout, ownership of q/k/v/o/lse and the other errors are
+ * fa_fwd_ex's.
  */
 int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
                    int64_t H, int64_t N, int64_t d, int causal, float scale, int fp16,

@@ -73,44 +73,57 @@ def test_kernel_hash_ignores_comments():
     assert re.fullmatch(r"[0-9a-f]{16}", bench.kernel_source_hash())
 
 
-def test_clock_samples_kept_only_inside_the_timed_region(tmp_path):
-    """The clock record of a bench line uses only the nvidia-smi samples whose
-    timestamps fall inside the timed region, and says so when none did."""
+def test_clock_samples_kept_only_inside_the_timed_region():
+    """The clock record of a bench line uses only the samples whose host
+    timestamps fall inside the timed region, and says so when none did;
+    reason bits decode to NVML's clock-event names."""
     sys.path.insert(0, ROOT)
-    import datetime
     import bench
 
-    class _Done:
-        def terminate(self):
-            pass
-
-        def wait(self, timeout=None):
-            return 0
-
-    def sampler_with(lines):
-        s = bench.ClockSampler(0)
-        s.out_path = str(tmp_path / "clocks.csv")
-        with open(s.out_path, "w") as f:
-            f.write("".join(lines))
-        s.fh = open(s.out_path, "a")
-        s.proc = _Done()
-        return s
-
-    t0 = datetime.datetime(2026, 1, 2, 3, 4, 5)
-    def row(dt_s, mhz, watts, power_cap):
-        ts = (t0 + datetime.timedelta(seconds=dt_s)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
-        cap = "Active" if power_cap else "Not Active"
-        return f"{ts}, 0, {mhz}, 2070, {watts}, 0x4, Not Active, Not Active, Not Active, {cap}\n"
-
-    lines = [row(0.0, 2070, 120, False), row(1.0, 1800, 1390, True), row(1.2, 1820, 1388, True),
-             row(1.4, 1790, 1391, True), row(3.0, 2070, 150, False)]
-    window = ((t0 + datetime.timedelta(seconds=0.9)).timestamp(),
-              (t0 + datetime.timedelta(seconds=1.5)).timestamp())
-    rec = sampler_with(lines).stop(window=window)
+    s = bench.ClockSampler(reader=lambda: None)
+    s.samples = [(0.0, 2070.0, 2070.0, 120.0, 0x0), (1.0, 1800.0, 2070.0, 1390.0, 0x4),
+                 (1.2, 1820.0, 2070.0, 1388.0, 0x4), (1.4, 1790.0, 2070.0, 1391.0, 0x4 | 0x1),
+                 (3.0, 2070.0, 2070.0, 150.0, 0x0)]
+    rec = s.stop(window=(0.9, 1.5))
     assert rec["samples"] == 3 and rec["sampled"] == "timed region"
     assert rec["sm_mhz"] == 1800 and rec["power_w_max"] == 1391
     assert rec["reasons"] == ["sw_power_cap"]
     # a window that no sample falls in: the whole run, marked as such
-    far = (window[0] + 100, window[1] + 100)
-    rec = sampler_with(lines).stop(window=far)
+    rec = s.stop(window=(100.0, 101.0))
     assert rec["samples"] == 5 and rec["sampled"].startswith("whole run")
+    s.samples = [(1.0, 1500.0, 2070.0, 1300.0, 0x8 | 0x20 | 0x40)]
+    rec = s.stop(window=(0.0, 2.0))
+    assert rec["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
+
+
+def test_clock_sampler_thread_polls_during_a_window():
+    """The background thread reads the clock source repeatedly: a 60 ms
+    window at the 2 ms period holds many samples."""
+    sys.path.insert(0, ROOT)
+    import time as _time
+    import bench
+
+    s = bench.ClockSampler(reader=lambda: (1965.0, 2070.0, 900.0, 0x4), period_s=0.002)
+    s.start()
+    _time.sleep(0.02)
+    t0 = _time.time()
+    _time.sleep(0.06)
+    t1 = _time.time()
+    rec = s.stop(window=(t0, t1))
+    assert rec["sampled"] == "timed region" and rec["samples"] >= 5
+    assert rec["sm_mhz"] == 1965.0 and rec["reasons"] == ["sw_power_cap"]
+    assert bench.ClockSampler(reader=None).stop()["reasons"] == ["NVML unavailable"]
+
+
+def test_default_workload_is_the_largest_bf16_shape():
+    """The line the benchmark prints by default is on the largest bf16
+    target shape (the long causal sequence), and a profile summary name is
+    derived from the workload it covers."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from attn_inputs import WORKLOADS
+    w = WORKLOADS[bench.DEFAULT_WORKLOAD]
+    bf16 = [x for x in WORKLOADS.values() if x.dtype == "bf16"]
+    assert w.flops() == max(x.flops() for x in bf16 if x.name != "b16h32n8192d128_causal")
+    assert (w.B, w.H, w.N, w.d, w.causal) == (1, 32, 16384, 128, True)
+    assert bench.profile_summary(w.name).endswith("fa_fwd_kernel_b1h32n16384d128_causal.md")

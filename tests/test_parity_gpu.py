@@ -286,6 +286,17 @@ def test_cuda_graph_capture_replays_bitwise(B, H, N, causal):
     assert fa().fa_get_status() == 0
 
 
+@pytest.mark.parametrize("fn", ["fa_fwd", "fa_fwd_ex"])
+def test_split_calls_after_setup_allocate_nothing(fn):
+    """The caller owns every buffer and, once the device is set up (the
+    first call reserves the split-scratch pool), calls issued on one stream
+    allocate no device memory: in a fresh process, after a causal first
+    call, ten split calls leave free device memory unchanged."""
+    from tests.fresh_process import free_memory_around_split_calls
+    free0, free1 = free_memory_around_split_calls(fn)
+    assert free1 == free0
+
+
 def test_concurrent_streams_split_scratch():
     """Calls on two streams at once, each with a split last round, take
     separate scratch from the stream-ordered pool: both match their serial
