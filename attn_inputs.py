@@ -70,6 +70,11 @@ WORKLOADS = {
     # device): a case small enough for a full profiler capture
     "b2h32n8192d128_fp16_peaked": Workload("b2h32n8192d128_fp16_peaked", 2, 32, 8192, 128,
                                            "fp16", False, k_mult=4.0, index=4),
+    # d=64 with long items (32 K/V blocks per Q tile), both masks: the
+    # head dim's steady state rather than its launch and ramp; not target shapes
+    "b4h32n4096d64": Workload("b4h32n4096d64", 4, 32, 4096, 64, "bf16", False, index=6),
+    "b4h32n4096d64_causal": Workload("b4h32n4096d64_causal", 4, 32, 4096, 64, "bf16", True,
+                                     index=6),
     # a large causal batch (K and V: 2 GiB, far beyond L2): the case the
     # head-by-head causal order is for; not one of the target shapes
     "b16h32n8192d128_causal": Workload("b16h32n8192d128_causal", 16, 32, 8192, 128, "bf16",

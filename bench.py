@@ -1,7 +1,9 @@
 """Throughput benchmark of the attention forward on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME]
+                    [--workload NAME] [--variant stages=S,exp_split=E]
+    python bench.py --sweep [--workload NAME] [--steps K] [--sweep-reps R]
+    python bench.py --rescale-stats [--workload NAME]
 
 A step is one forward (O and LSE) over the whole workload; by default the
 largest bf16 shape of the target set, the long causal sequence
@@ -28,6 +30,15 @@ GPU (heads are independent: weak scaling, no data-path collective).
 host->device, runs the forward and copies O and LSE back, all inside the
 timed region (the library overlaps the copies of one chunk of heads with
 the forward of another).
+
+`--variant` times one of the library's kernel variants (fa_fwd_variant:
+K/V ring depth, share of exponentials on the FMA pipes) instead of the
+default.  `--sweep` times every variant built for the workload's head dim
+and dtype, R rounds in alternating order, and prints a Markdown table of
+median TFLOPS, median SM clock and FLOP per SM clock (the clock-normalised
+rate, which removes the power limit's effect on the clock).
+`--rescale-stats` runs the counting build once and prints how often the
+online softmax's O rescale fired.
 
 `--impl reference` times the CPU oracle (the reference arm: a plain fp64
 C implementation of the definition) on the host cores, each step a bounded
@@ -376,6 +387,10 @@ def run_ours(args, w):
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     call = fa.fa_fwd if w.dtype == "bf16" else fa.fa_fwd_fp16
+    variant = parse_variant(args.variant)
+    if variant:
+        def call(q, k, v, o, lse, causal, stream):  # noqa: F811
+            fa.fa_fwd_variant(q, k, v, o, lse, causal=causal, stream=stream, **variant)
     stream = torch.cuda.current_stream(dev)
     flops = w.flops()
 
@@ -494,7 +509,7 @@ def run_ours(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic",
         "config": dict(w.describe(), parallelism=f"replicas{world}" if world > 1 else "single",
-                       l2=l2_note(w)),
+                       l2=l2_note(w), **({"variant": variant} if variant else {})),
         "gpu_launches": args.steps,
         "clocks": clocks,
         "roofline": roofline,
@@ -505,6 +520,114 @@ def run_ours(args, w):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+    return 0
+
+
+def parse_variant(text):
+    """'stages=3,exp_split=4' -> {"stages": 3, "exp_split": 4} (None/'' -> {})."""
+    out = {}
+    for part in (text or "").split(","):
+        if not part.strip():
+            continue
+        key, _, val = part.partition("=")
+        key = key.strip()
+        if key not in ("stages", "exp_split", "causal_order"):
+            raise ValueError(f"unknown variant key {key!r} (stages, exp_split, causal_order)")
+        out[key] = int(val)
+    return out
+
+
+def run_sweep(args, w):
+    """Time every kernel variant built for the workload's head dim and
+    dtype (the default first), `args.sweep_reps` rounds with the order
+    reversed every other round; print a Markdown table of medians."""
+    import torch
+
+    import exact_attention_forward_07_gb300 as fa
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    q, k, v = (x.to(dev) for x in make_workload_inputs(w))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    fp16 = int(w.dtype == "fp16")
+    cands = [dict(stages=x["stages"], exp_split=x["exp_split"], causal_order=fa.FA_ORDER_AUTO)
+             for x in fa.variants() if x["d"] == w.d and x["fp16"] == fp16 and not x["stats"]]
+    if w.causal:  # the default kernel under each causal item order
+        cands += [dict(cands[0], causal_order=o) for o in (-1, 0)]
+    stream = torch.cuda.current_stream(dev)
+    steps = args.steps or 100
+    sampler = ClockSampler.for_device(dev.index)
+    sampler.start()
+    results = {i: [] for i in range(len(cands))}
+    for rep in range(args.sweep_reps):
+        order = list(range(len(cands)))
+        if rep % 2:
+            order.reverse()
+        for i in order:
+            kw = cands[i]
+            for _ in range(args.warmup):
+                fa.fa_fwd_variant(q, k, v, o, lse, causal=w.causal, stream=stream, **kw)
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0 = time.time()
+            e0.record(stream)
+            for _ in range(steps):
+                fa.fa_fwd_variant(q, k, v, o, lse, causal=w.causal, stream=stream, **kw)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            t1 = time.time()
+            if fa.fa_get_status(stream) != 0:
+                raise RuntimeError(f"kernel status error in variant {kw}")
+            ms = e0.elapsed_time(e1) / steps
+            mhz = [s[1] for s in sampler.samples if t0 <= s[0] <= t1 and s[1]]
+            results[i].append((w.flops() / (ms * 1e-3) / 1e12, ms,
+                               statistics.median(mhz) if mhz else None))
+    sampler.stop()
+    print(f"Sweep on {w.name} ({w.dtype}, {'causal' if w.causal else 'non-causal'}), "
+          f"{args.sweep_reps} rounds x {steps} launches per variant, medians:\n")
+    print("| stages | exp_split | causal order | TFLOPS | ms | SM MHz | FLOP/clk/SM |")
+    print("|---|---|---|---|---|---|---|")
+    for i, x in enumerate(cands):
+        order = {fa.FA_ORDER_AUTO: "auto", -1: "heaviest first"}.get(
+            x["causal_order"], f"head by head, {x['causal_order']} tail heads")
+        order = order if w.causal else "-"
+        tf = statistics.median(r[0] for r in results[i])
+        ms = statistics.median(r[1] for r in results[i])
+        clk = [r[2] for r in results[i] if r[2]]
+        mhz = statistics.median(clk) if clk else None
+        fpc = w.flops() / (ms * 1e-3 * mhz * 1e6 * n_sm) if mhz else None
+        print(f"| {x['stages']} | {x['exp_split']} | {order} | {tf:.1f} | {ms:.4f} | "
+              f"{mhz if mhz else 'n/a'} | {fpc:.0f} |" if fpc else
+              f"| {x['stages']} | {x['exp_split']} | {order} | {tf:.1f} | {ms:.4f} | n/a | n/a |")
+    return 0
+
+
+def run_rescale_stats(args, w):
+    """Run the counting build once on the workload and print how often the
+    O rescale fired (JSON)."""
+    import torch
+
+    import exact_attention_forward_07_gb300 as fa
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q, k, v = (x.to(dev) for x in make_workload_inputs(w))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    out = {"workload": w.name}
+    for thr in (8.0, 0.0):
+        stats = torch.zeros(4, dtype=torch.int64, device=dev)
+        fa.fa_fwd_variant(q, k, v, o, lse, causal=w.causal, rescale_threshold=thr, stats=stats)
+        torch.cuda.synchronize(dev)
+        if fa.fa_get_status() != 0:
+            raise RuntimeError("kernel status error in the counting build")
+        need, rows, wres, wblk = (int(x) for x in stats.cpu())
+        out[f"tau={thr:g}"] = {
+            "row_blocks_after_first": rows, "rows_rescaled": need,
+            "row_rescale_rate": need / rows if rows else None,
+            "warp_blocks_after_first": wblk, "warp_blocks_rescaling": wres,
+            "warp_rescale_rate": wres / wblk if wblk else None}
+    print(json.dumps(out), flush=True)
     return 0
 
 
@@ -522,6 +645,12 @@ def main(argv=None):
     ap.add_argument("--e2e-chunks", type=int, default=8)
     ap.add_argument("--cpu-heads", type=int, default=0,
                     help="heads in the cpu_baseline sample (0: about 1.1e12 FLOP of them)")
+    ap.add_argument("--variant", default="",
+                    help="kernel variant, e.g. stages=3,exp_split=4 (fa_fwd_variant)")
+    ap.add_argument("--sweep", action="store_true", help="time every built variant")
+    ap.add_argument("--sweep-reps", type=int, default=3)
+    ap.add_argument("--rescale-stats", action="store_true",
+                    help="count the O rescales of the workload (counting build)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
@@ -533,6 +662,10 @@ def main(argv=None):
             print(f"note: --gpus {args.gpus} but WORLD_SIZE={world}; using WORLD_SIZE",
                   file=sys.stderr)
     w = WORKLOADS[args.workload]
+    if args.sweep:
+        return run_sweep(args, w)
+    if args.rescale_stats:
+        return run_rescale_stats(args, w)
     if args.impl == "reference":
         if args.steps is None:
             args.steps = 500

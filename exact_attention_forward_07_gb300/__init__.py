@@ -16,8 +16,9 @@ import ctypes
 import math
 import os
 
-__all__ = ["FaError", "fa_fwd_host", "fa_fwd_noalloc", "fa_fwd", "fa_fwd_fp16", "fa_fwd_ex", "fa_get_status",
-           "fa_strerror", "fa_version", "forward", "library_path", "lib"]
+__all__ = ["FaError", "fa_fwd_host", "fa_fwd_noalloc", "fa_fwd", "fa_fwd_fp16", "fa_fwd_ex",
+           "fa_fwd_variant", "fa_get_status", "fa_strerror", "fa_version", "forward",
+           "library_path", "lib", "variants"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
@@ -41,6 +42,7 @@ FA_HOST_DEFAULT_CHUNKS = 8
 FA_HOST_MAX_CHUNKS = 1024
 FA_DEFAULT_RESCALE_THRESHOLD = 8.0
 FA_MAX_RESCALE_THRESHOLD = 12.0
+FA_ORDER_AUTO = -2
 
 _lib = None
 
@@ -77,6 +79,15 @@ def lib():
         L.fa_fwd_ex.restype = ctypes.c_int
         L.fa_fwd_noalloc.argtypes = L.fa_fwd_ex.argtypes
         L.fa_fwd_noalloc.restype = ctypes.c_int
+        L.fa_fwd_variant.argtypes = [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int,
+                                     ctypes.c_float, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, P, P]
+        L.fa_fwd_variant.restype = ctypes.c_int
+        L.fa_variant_count.argtypes = []
+        L.fa_variant_count.restype = ctypes.c_int
+        IP = ctypes.POINTER(ctypes.c_int)
+        L.fa_variant_info.argtypes = [ctypes.c_int, IP, IP, IP, IP, IP]
+        L.fa_variant_info.restype = ctypes.c_int
         L.fa_fwd_host.argtypes = [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int, ctypes.c_float,
                                   ctypes.c_int, ctypes.c_int]
         L.fa_fwd_host.restype = ctypes.c_int
@@ -179,6 +190,47 @@ def fa_fwd_noalloc(q, k, v, o, lse, causal=False, scale=None, rescale_threshold=
     fp16 = int(q.dtype == torch.float16)
     _call("fa_fwd_noalloc", q, k, v, o, lse, causal, scale, stream, q.dtype,
           extra=(fp16, float(rescale_threshold)))
+
+
+def fa_fwd_variant(q, k, v, o, lse, causal=False, scale=None, rescale_threshold=None,
+                   stages=0, exp_split=0, causal_order=FA_ORDER_AUTO, stats=None,
+                   stream=None) -> None:
+    """Forward through one of the library's kernel variants (tuning and
+    measurement): `stages` K/V ring slots (0 = default), every
+    `exp_split`-th pair of exponentials on the FMA pipes (0 = none), a
+    forced causal item order (-1, or g >= 0 tail heads; default: the
+    library's choice), and optional rescale counters `stats` (a CUDA int64
+    tensor of 4, added to).  dtype from q (bf16/fp16)."""
+    import torch
+    if rescale_threshold is None:
+        rescale_threshold = FA_DEFAULT_RESCALE_THRESHOLD
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"unsupported dtype {q.dtype}: use bfloat16 or float16")
+    sp = None
+    if stats is not None:
+        if not (stats.is_cuda and stats.dtype == torch.int64 and stats.numel() == 4
+                and stats.is_contiguous()):
+            raise ValueError("stats must be a contiguous CUDA int64 tensor of 4 counters")
+        sp = stats.data_ptr()
+    fp16 = int(q.dtype == torch.float16)
+    _call("fa_fwd_variant", q, k, v, o, lse, causal, scale, stream, q.dtype,
+          extra=(fp16, float(rescale_threshold), int(stages), int(exp_split),
+                 int(causal_order), sp))
+
+
+def variants():
+    """The kernel variants built into the library: a list of dicts with d,
+    fp16, stages, exp_split and stats."""
+    out = []
+    L = lib()
+    vals = [ctypes.c_int() for _ in range(5)]
+    for i in range(L.fa_variant_count()):
+        rc = L.fa_variant_info(i, *[ctypes.byref(x) for x in vals])
+        if rc != FA_OK:
+            raise FaError(rc, "fa_variant_info")
+        out.append(dict(zip(("d", "fp16", "stages", "exp_split", "stats"),
+                            (x.value for x in vals))))
+    return out
 
 
 def fa_get_status(stream=None) -> int:

@@ -21,6 +21,8 @@ __device__ unsigned g_fa_status = 0;  // per-device status word (FA_ERR_TIMEOUT 
 __device__ __align__(256) unsigned char g_fa_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxVariants = 32;
+constexpr int kOrderAuto = -2;  // causal item order: the library's choice
 
 struct DeviceState {
   std::once_flag once;
@@ -34,7 +36,7 @@ struct DeviceState {
   // causal item order chosen per (B*H, Q tiles): the host simulation runs
   // once per shape
   std::mutex order_mu;
-  std::unordered_map<uint64_t, bool> order_cache;
+  std::unordered_map<uint64_t, int> order_cache;  // causal_order's result
   // fa_fwd_host: copy-in, compute and copy-out streams, events and device
   // staging memory (created on first use, staging grown as needed); calls
   // on one device take host_mu, so they run one at a time
@@ -45,8 +47,8 @@ struct DeviceState {
   cudaEvent_t host_ev[3][3] = {};  // [slot][loaded, done, drained]
   uint8_t *stage = nullptr;
   size_t stage_bytes = 0;
-  std::once_flag attr_once[4];
-  int attr_err[4] = {0, 0, 0, 0};
+  std::once_flag attr_once[kMaxVariants];  // shared-memory attribute, per kernel variant
+  int attr_err[kMaxVariants] = {};
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -205,15 +207,20 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 // heaviest pairs first across all heads balances the SMs best, but once the
 // heads' K/V outgrow L2 it reads a head's K/V from HBM again for each of its
 // pairs; head by head (heaviest pair first within each head) keeps a head's
-// K/V in L2 across its pairs.  Both orders' per-CTA load is simulated (the
-// larger tile's K/V blocks per item, plus about 1.3 blocks for the restart
-// between items) and head by head is taken unless it balances more than 8
-// percentage points worse: under the board's power limit the HBM re-reads
-// cost clock speed, which outweighs a few points of balance.  Large
-// launches (over 2^20 items) keep the first order.
-bool causal_head_major(int BH, int n_qtiles, int n_pairs, int G) {
+// K/V in L2 across its pairs, but leaves the last head's heavy pairs to end
+// the launch.  So head by head takes its last g heads together, heaviest
+// pair first across them (their K/V, at most 96 MiB, still fits in L2),
+// with g chosen among a few sizes for the best balance.  The per-CTA load
+// of each order is simulated (the larger tile's K/V blocks per item, plus
+// about 1.3 blocks for the restart between items); head by head is taken
+// unless it balances more than 8 percentage points worse than heaviest
+// first across all heads: under the board's power limit the HBM re-reads
+// cost clock speed, which outweighs a few points of balance.  Launches over
+// 2^20 items keep the first order.  Returns -1 (heaviest first across all
+// heads) or g >= 0 (head by head, g tail heads).
+int causal_order(int BH, int n_qtiles, int n_pairs, int G, double kv_head_bytes) {
   const int64_t n = static_cast<int64_t>(BH) * n_pairs;
-  if (n <= G || n > (int64_t(1) << 20)) return false;
+  if (n <= G || n > (int64_t(1) << 20)) return -1;
   // load of one item of each level (level 0 = the heaviest pair)
   std::vector<double> w(static_cast<size_t>(n_pairs));
   for (int level = 0; level < n_pairs; ++level) {
@@ -221,19 +228,28 @@ bool causal_head_major(int BH, int n_qtiles, int n_pairs, int G) {
     w[static_cast<size_t>(level)] = (qt1 < n_qtiles ? qt1 + 1 : qt1) + 1.3;
   }
   std::vector<double> load(static_cast<size_t>(G));
-  auto balance = [&](bool head_major) {
+  // g < 0: heaviest first across all heads; g >= 0: head by head, g tail heads
+  auto balance = [&](int g) {
     std::fill(load.begin(), load.end(), 0.0);
-    int level = 0, head = 0;  // of item i, in the order simulated
+    const int64_t first = g < 0 ? 0 : static_cast<int64_t>(BH - g) * n_pairs;
+    const int width = g < 0 ? BH : g;  // heads taken together, level by level
+    int level = 0, col = 0;            // of item i in the level-by-level part
+    int hm_level = 0;                  // of item i in the head-by-head part
     int64_t i = 0;
     for (int64_t r = 0; i < n; ++r) {
       for (int off = 0; off < G && i < n; ++off, ++i) {
-        load[static_cast<size_t>((r & 1) ? G - 1 - off : off)] += w[static_cast<size_t>(level)];
-        if (head_major) {
-          if (++level == n_pairs) level = 0;
-        } else if (++head == BH) {
-          head = 0;
-          ++level;
+        int lv;
+        if (i < first) {
+          lv = hm_level;
+          if (++hm_level == n_pairs) hm_level = 0;
+        } else {
+          lv = level;
+          if (++col == width) {
+            col = 0;
+            ++level;
+          }
         }
+        load[static_cast<size_t>((r & 1) ? G - 1 - off : off)] += w[static_cast<size_t>(lv)];
       }
     }
     double sum = 0.0, mx = 0.0;
@@ -243,15 +259,25 @@ bool causal_head_major(int BH, int n_qtiles, int n_pairs, int G) {
     }
     return sum / G / mx;
   };
-  return balance(true) >= balance(false) - 0.08;
+  int best_g = 0;
+  double best = balance(0);
+  for (int g : {2, 4, 6, 8, 12, 16, 24, 32}) {
+    if (g >= BH || g * kv_head_bytes > 96.0 * 1024 * 1024) break;
+    const double b = balance(g);
+    if (b > best + 1e-9) {
+      best = b;
+      best_g = g;
+    }
+  }
+  return best >= balance(-1) - 0.08 ? best_g : -1;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, int STAGES, int EXPSPLIT, bool STATS>
 int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *v, void *o,
            float *lse, int64_t BH, int64_t N, int causal, float scale, float thr, bool noalloc,
-           cudaStream_t stream) {
-  using C = fa::Cfg<D, BF16>;
-  auto kernel = fa::fa_fwd_kernel<D, BF16>;
+           unsigned long long *stats, int order, cudaStream_t stream) {
+  using C = fa::Cfg<D, BF16, STAGES, EXPSPLIT, STATS>;
+  auto kernel = fa::fa_fwd_kernel<D, BF16, STAGES, EXPSPLIT, STATS>;
   std::call_once(ds.attr_once[slot], [&] {
     cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -278,20 +304,26 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
   // K and V of all heads beyond 64 MiB: L2 (126 MB) no longer holds them
   const double kv_bytes = 2.0 * static_cast<double>(BH) * static_cast<double>(N) * D * 2.0;
   p.causal_head_major = 0;
+  p.causal_tail_heads = 0;
   if (causal && kv_bytes > 64.0 * 1024 * 1024) {
     const uint64_t key = (static_cast<uint64_t>(p.BH) << 32) | static_cast<uint32_t>(p.n_qtiles);
     std::lock_guard<std::mutex> lock(ds.order_mu);
     auto hit = ds.order_cache.find(key);
     if (hit == ds.order_cache.end()) {
       if (ds.order_cache.size() >= 4096) ds.order_cache.clear();  // bounded
-      hit = ds.order_cache
-                .emplace(key, causal_head_major(p.BH, p.n_qtiles, p.n_pairs, ds.sm_count))
-                .first;
+      const int g = causal_order(p.BH, p.n_qtiles, p.n_pairs, ds.sm_count, kv_bytes / BH);
+      hit = ds.order_cache.emplace(key, g).first;
     }
-    p.causal_head_major = hit->second ? 1 : 0;
+    p.causal_head_major = hit->second >= 0 ? 1 : 0;
+    p.causal_tail_heads = hit->second >= 0 ? hit->second : 0;
+  }
+  if (causal && order != kOrderAuto) {  // fa_fwd_variant's override
+    p.causal_head_major = order >= 0 ? 1 : 0;
+    p.causal_tail_heads = order >= 0 ? order : 0;
   }
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.rescale_thr = thr;
+  p.stats = stats;
 
   // Wave-tail split.  With G persistent CTAs, the last round holds
   // R = n_items mod G items and leaves G - R SMs idle; when R <= G / 2 each
@@ -374,9 +406,57 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
   return FA_OK;
 }
 
+// Kernel variants built into the library.  The first entry of each (d,
+// dtype) is the one the product entry points use; the others are the ring
+// depths, exp splits and the rescale counter that fa_fwd_variant reaches
+// for tuning and measurement.
+typedef int (*LaunchFn)(DeviceState &, int, const void *, const void *, const void *, void *,
+                        float *, int64_t, int64_t, int, float, float, bool,
+                        unsigned long long *, int, cudaStream_t);
+struct Variant {
+  int d;
+  bool bf16;
+  int stages;     // K/V ring slots (the resolved count)
+  int exp_split;  // every exp_split-th pair of exponentials on the FMA pipes (0: none)
+  bool stats;
+  LaunchFn fn;
+};
+#define FA_V(DD, BB, ST, SP, STATS) \
+  Variant{DD, BB, fa::Cfg<DD, BB, ST, SP, STATS>::kStages, SP, STATS, launch<DD, BB, ST, SP, STATS>}
+const Variant kVariants[] = {
+    // defaults (product entry points)
+    FA_V(64, true, 0, 0, false), FA_V(64, false, 0, 0, false),
+    FA_V(128, true, 0, 0, false), FA_V(128, false, 0, 0, false),
+    // d = 128 ring depths and exp splits
+    FA_V(128, true, 2, 0, false), FA_V(128, true, 3, 0, false),
+    FA_V(128, true, 0, 4, false), FA_V(128, true, 0, 2, false),
+    FA_V(128, false, 3, 0, false),
+    // d = 64 ring depths and exp splits
+    FA_V(64, true, 4, 0, false), FA_V(64, true, 6, 0, false), FA_V(64, true, 10, 0, false),
+    FA_V(64, true, 0, 4, false), FA_V(64, true, 0, 2, false),
+    // rescale counters at the default configuration
+    FA_V(64, true, 0, 0, true), FA_V(128, true, 0, 0, true), FA_V(128, false, 0, 0, true),
+};
+#undef FA_V
+constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
+static_assert(kNumVariants <= kMaxVariants, "more variants than per-device attribute slots");
+
+// Index of the variant, or -1.  stages 0 = the default ring depth.
+int find_variant(int d, bool bf16, int stages, int exp_split, bool stats) {
+  for (int i = 0; i < kNumVariants; ++i) {
+    const Variant &x = kVariants[i];
+    const int def_stages = kVariants[(d == 64 ? 0 : 2) + (bf16 ? 0 : 1)].stages;
+    if (x.d == d && x.bf16 == bf16 && x.stages == (stages ? stages : def_stages) &&
+        x.exp_split == exp_split && x.stats == stats)
+      return i;
+  }
+  return -1;
+}
+
 int fwd_common(bool bf16, const void *q, const void *k, const void *v, void *o, float *lse,
                int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
-               float thr, fa_stream_t stream, bool noalloc = false) {
+               float thr, fa_stream_t stream, bool noalloc = false, int variant = -1,
+               unsigned long long *stats = nullptr, int order = kOrderAuto) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_HEADDIM;
@@ -396,17 +476,16 @@ int fwd_common(bool bf16, const void *q, const void *k, const void *v, void *o, 
   for (const void *in : {q, k, v})
     if (overlaps(o, tbytes, in, tbytes) || overlaps(lse, lbytes, in, tbytes)) return FA_ERR_ALIAS;
   if (overlaps(o, tbytes, lse, lbytes)) return FA_ERR_ALIAS;
+  if (variant < 0) variant = (d == 64 ? 0 : 2) + (bf16 ? 0 : 1);  // the default variants
+  if (kVariants[variant].d != d || kVariants[variant].bf16 != bf16) return FA_ERR_OPTION;
+  if (order != kOrderAuto && (order < -1 || order > BH)) return FA_ERR_OPTION;
 
   DeviceState *ds = nullptr;
   int rc = device_state(&ds);
   if (rc != FA_OK) return rc;
   if (!noalloc) ensure_pool(*ds, ds->dev);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-#define FA_LAUNCH(DD, BB, SLOT) \
-  launch<DD, BB>(*ds, SLOT, q, k, v, o, lse, BH, N, causal, scale, thr, noalloc, st)
-  if (d == 64) return bf16 ? FA_LAUNCH(64, true, 0) : FA_LAUNCH(64, false, 1);
-  return bf16 ? FA_LAUNCH(128, true, 2) : FA_LAUNCH(128, false, 3);
-#undef FA_LAUNCH
+  return kVariants[variant].fn(*ds, variant, q, k, v, o, lse, BH, N, causal, scale, thr, noalloc,
+                               stats, order, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -438,6 +517,43 @@ int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *
                    float rescale_threshold, fa_stream_t stream) {
   return fwd_common(fp16 == 0, q, k, v, o, lse, B, H, N, d, causal, scale, rescale_threshold,
                     stream, /*noalloc=*/true);
+}
+
+int fa_fwd_variant(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                   int64_t H, int64_t N, int64_t d, int causal, float scale, int fp16,
+                   float rescale_threshold, int stages, int exp_split, int causal_order,
+                   unsigned long long *stats, fa_stream_t stream) {
+  if (d != 64 && d != 128) return d < 1 ? FA_ERR_SHAPE : FA_ERR_HEADDIM;
+  const int idx = find_variant(static_cast<int>(d), fp16 == 0, stages, exp_split, stats != nullptr);
+  if (idx < 0) return FA_ERR_OPTION;
+  if (stats != nullptr && (reinterpret_cast<uintptr_t>(stats) & 7u)) return FA_ERR_ALIGN;
+  return fwd_common(fp16 == 0, q, k, v, o, lse, B, H, N, d, causal, scale, rescale_threshold,
+                    stream, /*noalloc=*/false, idx, stats, causal_order);
+}
+
+int fa_variant_count(void) { return kNumVariants; }
+
+int fa_causal_order(int64_t B, int64_t H, int64_t N, int64_t d, int sm_count) {
+  if (B < 1 || H < 1 || N < 1 || N > FA_MAX_N || sm_count < 1) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  const int64_t BH = B * H;
+  if (BH * ((N + 255) / 256) > INT32_MAX / 2) return FA_ERR_SHAPE;
+  const int n_qtiles = static_cast<int>((N + 127) / 128), n_pairs = (n_qtiles + 1) / 2;
+  const double kv_bytes = 2.0 * static_cast<double>(BH) * static_cast<double>(N) * d * 2.0;
+  if (kv_bytes <= 64.0 * 1024 * 1024) return -1;
+  return causal_order(static_cast<int>(BH), n_qtiles, n_pairs, sm_count, kv_bytes / BH);
+}
+
+int fa_variant_info(int index, int *d, int *fp16, int *stages, int *exp_split, int *stats) {
+  if (index < 0 || index >= kNumVariants) return FA_ERR_OPTION;
+  if (!d || !fp16 || !stages || !exp_split || !stats) return FA_ERR_NULL;
+  const Variant &x = kVariants[index];
+  *d = x.d;
+  *fp16 = x.bf16 ? 0 : 1;
+  *stages = x.stages;
+  *exp_split = x.exp_split;
+  *stats = x.stats ? 1 : 0;
+  return FA_OK;
 }
 
 // Pipelined forward on host buffers: heads in chunks; chunk c+1 is copied

@@ -71,6 +71,7 @@ struct Params {
   int n_items;       // BH * n_pairs
   int causal;
   int causal_head_major;  // causal item order: 0 heaviest pair first across heads, 1 head by head
+  int causal_tail_heads;  // head by head: the last this many heads go heaviest pair first across them
   float scale_log2;  // scale * log2(e)
   float rescale_thr; // rescale O only when the running max grows by more than this (log2 units)
   // Wave-tail split (non-causal only): the items from
@@ -84,15 +85,27 @@ struct Params {
   float4 *part_o;       // [piece][D / 4 column groups][256 rows] fp32 x 4
   float *part_st;       // [piece][3][256 rows]: max (log2 units), sum of P, corrected sum
   unsigned *part_cnt;   // [split item]: pieces finished (zero before the launch)
+  // rescale counters (kernel variants built with STATS only): [0] (row,
+  // block) pairs after a tile's first block whose running max grew past the
+  // threshold, [1] all such (row, block) pairs, [2] warp-blocks that ran
+  // the O rescale loop, [3] all warp-blocks after a tile's first block
+  unsigned long long *stats;
 };
 
-template <int D, bool BF16>
+// Kernel variants: STAGES = K/V ring slots (0: the default, 4 at d = 128
+// and 8 at d = 64), EXPSPLIT = every EXPSPLIT-th pair of the softmax's
+// exponentials is evaluated on the FMA pipes (exp2_poly2) instead of the
+// special-function unit (0: none), STATS = count rescales (Params::stats).
+template <int D, bool BF16, int STAGES = 0, int EXPSPLIT = 0, bool STATS = false>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
   static constexpr int kRows = 128;                   // Q rows per tile, keys per block
   static constexpr int kTileBytes = kRows * D * 2;    // one Q, K or V tile
   static constexpr int kHalfBytes = kRows * 64 * 2;   // 64 columns: one 128-byte swizzle span
-  static constexpr int kStages = (D == 128) ? 4 : 8;  // K/V ring slots
+  static constexpr int kStages = STAGES ? STAGES : ((D == 128) ? 4 : 8);  // K/V ring slots
+  static constexpr int kExpSplit = EXPSPLIT;
+  static constexpr bool kStats = STATS;
+  static_assert(kStages >= 2, "the ring needs two slots");
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
@@ -112,6 +125,7 @@ struct Cfg {
   // softmax row exchange: [tile][parity][half][value][row] floats, 8 KB
   static constexpr int kXchOff = (kMiscOff + 16 + 15) & ~15;
   static constexpr int kSmemBytes = kXchOff + 2 * 2 * 2 * 2 * 128 * 4 + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory beyond the per-CTA limit");
   static constexpr uint32_t kTmemCols = 512;
   // tensor-memory column of S_t, O_t and P_t for Q tile t: P_t is packed
   // 16-bit pairs over the first 64 columns of S_t (d = 128), or in its own
@@ -145,13 +159,24 @@ struct Item {
 // nearest the end of the sequence sees the most keys), across all heads --
 // or, where the host found that order no better balanced, head by head
 // (heaviest pair first within a head), which keeps each head's K/V in L2
-// for all of its pairs.
+// for all of its pairs; then the last causal_tail_heads heads are taken
+// together, heaviest pair first across them, so the light pairs of several
+// heads end the launch instead of one head's heavy ones.
 __device__ __forceinline__ Item decode_item(int item, const Params &p) {
   Item it;
   int pair;
   if (p.causal && p.causal_head_major) {
-    it.bh = item / p.n_pairs;
-    pair = p.n_pairs - 1 - (item - it.bh * p.n_pairs);
+    const int g = p.causal_tail_heads;
+    const int first = (p.BH - g) * p.n_pairs;
+    if (item < first) {
+      it.bh = item / p.n_pairs;
+      pair = p.n_pairs - 1 - (item - it.bh * p.n_pairs);
+    } else {
+      const int s = item - first;
+      const int level = s / g;
+      it.bh = p.BH - g + (s - level * g);
+      pair = p.n_pairs - 1 - level;
+    }
   } else if (p.causal) {
     const int level = item / p.BH;
     it.bh = item - level * p.BH;
@@ -248,6 +273,45 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// 2^x for a pair of x on the FMA pipes, for the share of the softmax's
+// exponentials taken off the special-function unit (the FlashAttention v4
+// Blackwell pipeline diagram, pseudo-code panel and v3 -> v4 comparison:
+// exp is emulated in software for part of the elements).  Cody-Waite
+// split x = n + f, n = round(x): adding 1.5 * 2^23 rounds x to an integer
+// and leaves n in the low mantissa bits of the sum, so those bits shifted
+// into the exponent field scale p(f) by 2^n.  p(f) ~ 2^f on [-1/2, 1/2] is
+// a minimax fit of the relative error (Remez exchange, computed by
+// fit_exp2_poly.py in this directory): degree 3 (7.5e-5) for bf16
+// probabilities, degree 4 (2.6e-6) for fp16.  x is clamped at -127 and a
+// result whose exponent would go below zero is flushed to +0 by an integer
+// max, so masked logits (-inf) give exactly 0 as the hardware ex2 does.
+template <bool BF16>
+__device__ __forceinline__ void exp2_poly2(uint64_t x2, float &e0, float &e1) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  float x0, x1;
+  f2_split(x2, x0, x1);
+  const uint64_t xc = f2(fmaxf(x0, -127.0f), fmaxf(x1, -127.0f));
+  const uint64_t t = fadd2(xc, f2(kRound, kRound));            // round(x) in the low bits
+  const uint64_t n = fadd2(t, f2(-kRound, -kRound));           // round(x), exactly
+  const uint64_t f = ffma2(n, f2(-1.0f, -1.0f), xc);            // x - n, exactly
+  uint64_t q;
+  if constexpr (BF16) {
+    q = ffma2(f, f2(5.517166853e-02f, 5.517166853e-02f), f2(2.426111251e-01f, 2.426111251e-01f));
+    q = ffma2(q, f, f2(6.932609677e-01f, 6.932609677e-01f));
+    q = ffma2(q, f, f2(9.999280572e-01f, 9.999280572e-01f));
+  } else {
+    q = ffma2(f, f2(9.570102207e-03f, 9.570102207e-03f), f2(5.591785908e-02f, 5.591785908e-02f));
+    q = ffma2(q, f, f2(2.402474433e-01f, 2.402474433e-01f));
+    q = ffma2(q, f, f2(6.931217909e-01f, 6.931217909e-01f));
+    q = ffma2(q, f, f2(9.999992847e-01f, 9.999992847e-01f));
+  }
+  float q0, q1, t0, t1;
+  f2_split(q, q0, q1);
+  f2_split(t, t0, t1);
+  e0 = __int_as_float(max(__float_as_int(q0) + (__float_as_int(t0) << 23), 0));
+  e1 = __int_as_float(max(__float_as_int(q1) + (__float_as_int(t1) << 23), 0));
+}
+
 // Stores a segment of NC 16-byte chunks (NC = 8: 128 bytes, NC = 4: 64
 // bytes) of each of a warp's 32 rows (lane = row) so that every store
 // instruction writes whole segments: within each group of NC lanes an NC x NC
@@ -283,11 +347,11 @@ __device__ __forceinline__ void store_rows(uint4 (&v)[NC], uint8_t *row0, size_t
   }
 }
 
-template <int D, bool BF16>
-__global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
+template <int D, bool BF16, int STAGES = 0, int EXPSPLIT = 0, bool STATS = false>
+__global__ void __launch_bounds__(Cfg<D, BF16, STAGES, EXPSPLIT, STATS>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
-  using C = Cfg<D, BF16>;
+  using C = Cfg<D, BF16, STAGES, EXPSPLIT, STATS>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte-swizzled tiles.
   const uint32_t raw = smem_u32(smem_raw);
@@ -707,6 +771,7 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
       if (q_idx < p.N && hf == 0) p.lse[row_off] = (M + lg2_approx(wl)) * 0.6931471805599453f;
     };
     const float sl2 = p.scale_log2;
+    uint32_t st_need = 0, st_rows = 0, st_wres = 0, st_wblk = 0;  // STATS only
     uint32_t s_par = 0, o_par = 0, xpar = 0;  // barrier phase bits, exchange parity
     uint32_t pv_par = 0;                      // PV done phase bit (d = 64)
     // bar.sync cannot time out, so a warp whose wait gave up (ok == false)
@@ -890,9 +955,17 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
             uint32_t pk[16];
 #pragma unroll
             for (int c = 32 * hh; c < 32 * hh + 32; c += 2) {
-              float x0, x1;
-              f2_split(ffma2(f2(s[c], s[c + 1]), sl2_2, negm_2), x0, x1);
-              const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+              const uint64_t x2 = ffma2(f2(s[c], s[c + 1]), sl2_2, negm_2);
+              float e0, e1;
+              if (C::kExpSplit > 0 && (c >> 1) % (C::kExpSplit > 0 ? C::kExpSplit : 1) ==
+                                          C::kExpSplit - 1) {
+                exp2_poly2<BF16>(x2, e0, e1);  // on the FMA pipes
+              } else {
+                float x0, x1;
+                f2_split(x2, x0, x1);
+                e0 = ex2_approx(x0);
+                e1 = ex2_approx(x1);
+              }
               pk[(c >> 1) & 15] = pack2<BF16>(e0, e1);
               sx2[(c >> 1) & 1] = fadd2(sx2[(c >> 1) & 1], f2(e0, e1));
             }
@@ -920,7 +993,18 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
           // m_new)").  PV_t(j-1) is complete -- its commit precedes S_t(j)'s
           // (d = 128), or its PV done was awaited above (d = 64) -- and
           // PV_t(j) waits for this block's signal.
+          if constexpr (C::kStats) {
+            if (j > 0) {
+              if (hf == 0) {
+                ++st_rows;
+                st_need += need ? 1u : 0u;
+              }
+              if (lane == 0) ++st_wblk;
+            }
+          }
           if (j > 0 && __any_sync(0xffffffffu, need)) {
+            if constexpr (C::kStats)
+              if (lane == 0) ++st_wres;
             const uint32_t tO = t_lane + C::col_o(t) + (D / 2) * hf;
             const uint64_t alpha2 = f2(alpha, alpha);
 #pragma unroll
@@ -966,6 +1050,15 @@ __global__ void __launch_bounds__(Cfg<D, BF16>::kThreads, 1)
         }
         softmax_sync();
         if (ok && *merge_flag && n > 0) merge(it, t);
+      }
+    }
+    if constexpr (C::kStats) {
+      unsigned long long v[4] = {st_need, st_rows, st_wres, st_wblk};  // widened once
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int sh = 16; sh >= 1; sh >>= 1) v[i] += __shfl_xor_sync(0xffffffffu, v[i], sh);
+        if (lane == 0 && p.stats != nullptr) atomicAdd(p.stats + i, v[i]);
       }
     }
     tc_fence_before();

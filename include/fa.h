@@ -80,6 +80,9 @@ typedef void *fa_stream_t;
 /* Bytes of the fixed device array that serves fa_fwd_noalloc's scratch. */
 #define FA_NOALLOC_SCRATCH_BYTES (16u << 20)
 
+/* fa_fwd_variant: let the library choose the causal item order. */
+#define FA_ORDER_AUTO (-2)
+
 /* Rescale threshold used by fa_fwd and fa_fwd_fp16, in log2 units of the
  * scaled logits (see fa_fwd_ex). */
 #define FA_DEFAULT_RESCALE_THRESHOLD 8.0f
@@ -169,6 +172,55 @@ int fa_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, 
 int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
                    int64_t H, int64_t N, int64_t d, int causal, float scale, int fp16,
                    float rescale_threshold, fa_stream_t stream);
+
+/*
+ * fa_fwd_variant -- the forward through one of the kernel variants built
+ * into the library, for tuning and measurement (the product entry points
+ * above always use the default variant of their head dim and dtype).
+ *
+ * The FlashAttention-from-scratch blog index (its auto-tuning post and the
+ * block-size trade-offs of its appendix) tunes a kernel's pipeline depth
+ * and tile shape per GPU; the FlashAttention v4 Blackwell pipeline diagram
+ * (pseudo-code panel, v3 -> v4 comparison) moves part of the softmax's
+ * exponentials from the special-function unit to the FMA pipes.  The
+ * variants expose those choices:
+ *   stages    : K/V ring slots in shared memory (0 = the default: 4 at
+ *               d = 128, 8 at d = 64)
+ *   exp_split : 0, or n: every n-th pair of the softmax's exponentials is
+ *               computed by a polynomial on the FMA pipes
+ *   causal_order : FA_ORDER_AUTO (the library's choice, see
+ *               fa_causal_order), or an order to force on causal launches:
+ *               -1 or g in [0, B*H] with fa_causal_order's meaning
+ *   stats     : NULL, or a DEVICE array of 4 unsigned 64-bit counters that
+ *               the kernel adds to (the caller zeroes it): [0] (row, K/V
+ *               block) pairs after a tile's first block where the running
+ *               max grew past the rescale threshold, [1] all such pairs,
+ *               [2] warp-blocks that ran the O rescale, [3] all warp-blocks
+ *               after a tile's first block.  Only the default ring depth
+ *               without exp split has a counting build.
+ * fa_variant_count / fa_variant_info list what is built (stages resolved
+ * to the actual slot count).  A combination that is not built gives
+ * FA_ERR_OPTION before anything is launched; all other arguments and
+ * errors are fa_fwd_ex's.  Every variant computes the same attention.
+ */
+int fa_fwd_variant(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                   int64_t H, int64_t N, int64_t d, int causal, float scale, int fp16,
+                   float rescale_threshold, int stages, int exp_split, int causal_order,
+                   unsigned long long *stats, fa_stream_t stream);
+int fa_variant_count(void);
+int fa_variant_info(int index, int *d, int *fp16, int *stages, int *exp_split, int *stats);
+
+/*
+ * fa_causal_order -- the order in which a causal launch of [B,H,N,d] on a
+ * GPU with sm_count SMs takes its work items (pairs of 128-row Q tiles),
+ * as the library chooses it (host computation only, no device call):
+ *   -1     heaviest pair first across all heads (also whenever K and V of
+ *          all heads total at most 64 MiB);
+ *   g >= 0 head by head, heaviest pair first within a head, with the last
+ *          g heads taken together, heaviest pair first across them.
+ * FA_ERR_SHAPE / FA_ERR_HEADDIM on bad arguments.  For tests and tuning.
+ */
+int fa_causal_order(int64_t B, int64_t H, int64_t N, int64_t d, int sm_count);
 
 /* Work split of fa_fwd_host. */
 #define FA_HOST_DEFAULT_CHUNKS 8

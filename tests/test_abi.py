@@ -145,3 +145,40 @@ def test_selftest_argument_errors(lib):
     assert lib.fa_selftest_wait_timeout(1000, None, None) == fa.FA_ERR_NULL
     assert lib.fa_selftest_wait_timeout(0, 0x10000000, None) == fa.FA_ERR_OPTION
     assert lib.fa_selftest_wait_timeout(2000000, 0x10000000, None) == fa.FA_ERR_OPTION
+
+
+def test_fa_fwd_variant_argument_errors(lib):
+    """Variants that are not built, and bad arguments, are refused before
+    any device call; every built variant is listed with a valid shape."""
+    def var(stages=0, exp_split=0, stats=None, order=fa.FA_ORDER_AUTO, **kw):
+        a = dict(q=Q, k=K, v=V, o=O, lse=L, B=1, H=1, N=128, d=128, causal=0, scale=0.125,
+                 fp16=0, thr=8.0)
+        a.update(kw)
+        return lib.fa_fwd_variant(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"],
+                                  a["N"], a["d"], a["causal"], a["scale"], a["fp16"], a["thr"],
+                                  stages, exp_split, order, stats, None)
+    assert var(stages=5) == fa.FA_ERR_OPTION        # no room for five 32 KiB slots
+    assert var(stages=7, d=64) == fa.FA_ERR_OPTION  # not built
+    assert var(exp_split=3) == fa.FA_ERR_OPTION
+    assert var(exp_split=4, fp16=1) == fa.FA_ERR_OPTION
+    assert var(stages=3, stats=0x10000000) == fa.FA_ERR_OPTION  # no counting build there
+    assert var(stats=0x10000004) == fa.FA_ERR_ALIGN
+    assert var(d=96) == fa.FA_ERR_HEADDIM
+    assert var(stages=3, q=None) == fa.FA_ERR_NULL
+    assert var(stages=3, thr=13.0) == fa.FA_ERR_OPTION
+    assert var(stages=3, o=Q) == fa.FA_ERR_ALIAS
+    assert var(order=-3) == fa.FA_ERR_OPTION
+    assert var(order=2, B=1, H=1) == fa.FA_ERR_OPTION  # more tail heads than heads
+    vs = fa.variants()
+    assert len(vs) == lib.fa_variant_count()
+    assert vs[:4] == [dict(d=64, fp16=0, stages=8, exp_split=0, stats=0),
+                      dict(d=64, fp16=1, stages=8, exp_split=0, stats=0),
+                      dict(d=128, fp16=0, stages=4, exp_split=0, stats=0),
+                      dict(d=128, fp16=1, stages=4, exp_split=0, stats=0)]
+    for x in vs:
+        assert x["d"] in (64, 128) and x["stages"] >= 2 and x["exp_split"] in (0, 2, 4)
+        # shared memory: Q tiles + ring within the 227 KiB a CTA may use
+        tile = 128 * x["d"] * 2
+        assert (2 + x["stages"]) * tile + 9 * 1024 <= 227 * 1024
+    i = ctypes.c_int()
+    assert lib.fa_variant_info(len(vs), *[ctypes.byref(i)] * 5) == fa.FA_ERR_OPTION

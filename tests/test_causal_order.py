@@ -1,0 +1,83 @@
+"""The host's choice of causal work-item order (no GPU needed).
+
+The library simulates, per shape, how the static rounds of its persistent
+grid load each SM under a few item orders, and picks one.  This restates
+that cost model independently in Python -- an item of two Q tiles costs the
+larger tile's K/V blocks plus 1.3 blocks of restart; round r gives item
+r*G + b to CTA b, reversed on odd rounds -- and checks that fa_causal_order
+returns the order the model prefers, over a spread of shapes and SM counts.
+"""
+import ctypes
+
+import pytest
+
+import exact_attention_forward_07_gb300 as fa
+from exact_attention_forward_07_gb300 import build as fa_build
+
+MIB = 1024 * 1024
+
+
+@pytest.fixture(scope="module")
+def order_fn():
+    fa_build.build()
+    f = fa.lib().fa_causal_order
+    f.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int]
+    f.restype = ctypes.c_int
+    return f
+
+
+def item_levels(BH, P, g):
+    """Level (0 = heaviest pair) of each item in launch order: g = None for
+    heaviest first across all heads, else head by head with the last g heads
+    taken level by level."""
+    if g is None:
+        return [i // BH for i in range(BH * P)]
+    first = (BH - g) * P
+    return [i % P if i < first else (i - first) // g for i in range(BH * P)]
+
+
+def balance(BH, T, G, g):
+    P = (T + 1) // 2
+    cost = []
+    for level in range(P):
+        qt1 = 2 * (P - 1 - level) + 1
+        cost.append((qt1 + 1 if qt1 < T else qt1) + 1.3)
+    load = [0.0] * G
+    for i, lv in enumerate(item_levels(BH, P, g)):
+        r, off = divmod(i, G)
+        load[G - 1 - off if r % 2 else off] += cost[lv]
+    return sum(load) / G / max(load)
+
+
+def expected(B, H, N, d, G):
+    BH, T = B * H, (N + 127) // 128
+    P = (T + 1) // 2
+    kv_head = 2 * N * d * 2
+    if BH * kv_head <= 64 * MIB or BH * P <= G or BH * P > 1 << 20:
+        return -1
+    best_g, best = 0, balance(BH, T, G, 0)
+    for g in (2, 4, 6, 8, 12, 16, 24, 32):
+        if g >= BH or g * kv_head > 96 * MIB:
+            break
+        b = balance(BH, T, G, g)
+        if b > best + 1e-9:
+            best_g, best = g, b
+    return best_g if best >= balance(BH, T, G, None) - 0.08 else -1
+
+
+SHAPES = [(1, 32, 16384, 128), (8, 16, 4096, 128), (16, 32, 8192, 128), (8, 64, 1024, 64),
+          (4, 16, 1024, 64), (1, 4, 65536, 128), (2, 8, 32768, 128), (4, 48, 4096, 64),
+          (2, 40, 8192, 128), (1, 96, 4000, 128), (3, 20, 12345, 64)]
+
+
+@pytest.mark.parametrize("G", [152, 148, 132])
+@pytest.mark.parametrize("B,H,N,d", SHAPES, ids=[f"b{b}h{h}n{n}d{d}" for b, h, n, d in SHAPES])
+def test_causal_order_matches_the_cost_model(order_fn, B, H, N, d, G):
+    assert order_fn(B, H, N, d, G) == expected(B, H, N, d, G)
+
+
+def test_causal_order_argument_errors(order_fn):
+    assert order_fn(0, 1, 128, 128, 152) == fa.FA_ERR_SHAPE
+    assert order_fn(1, 1, 128, 96, 152) == fa.FA_ERR_HEADDIM
+    assert order_fn(1, 1, 128, 128, 0) == fa.FA_ERR_SHAPE
+    assert order_fn(1, 32, 16384, 128, 152) == 12  # the long causal target shape

@@ -142,6 +142,33 @@ def test_parity_causal_head_by_head_order():
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
 
 
+TAIL_WINDOW_SHAPES = [(1, 32, 16384, 128), (8, 16, 4096, 128), (4, 48, 4096, 64)]
+
+
+@pytest.mark.parametrize("B,H,N,d", TAIL_WINDOW_SHAPES,
+                         ids=[f"b{b}h{h}n{n}d{d}" for b, h, n, d in TAIL_WINDOW_SHAPES])
+def test_parity_causal_tail_window_order(B, H, N, d):
+    """Causal launches taken head by head with their last heads taken
+    together (the host's choice for these shapes on a 152-SM GB300): one
+    seeded row of every (head, Q tile) is checked against the oracle, so a
+    work item that went missing or to the wrong head cannot pass."""
+    import ctypes
+    f = fa().lib().fa_causal_order
+    f.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int]
+    f.restype = ctypes.c_int
+    g = f(B, H, N, d, torch.cuda.get_device_properties(0).multi_processor_count)
+    q, k, v = make_qkv(B, H, N, d, torch.bfloat16, seed=4300 + N + H)
+    o, lse = run_gpu(q, k, v, True)
+    BH, tiles = B * H, N // 128
+    rng = np.random.default_rng(13)
+    rows = np.array([h * N + t * 128 + int(rng.integers(0, 128))
+                     for h in range(BH) for t in range(tiles)], dtype=np.int64)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, True, 1.0 / math.sqrt(d), rows=rows)
+    assert_close(o.reshape(BH * N, d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref,
+                 f"causal {B},{H},{N},{d} order {g}")
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+
+
 def test_uniform_attention_q_zero():
     """Q = 0: every visible key gets the same weight (closed form)."""
     q, k, v = make_qkv(1, 2, 300, 128, torch.bfloat16, seed=5, q_zero=True)
