@@ -540,7 +540,10 @@ def parse_variant(text):
 def run_sweep(args, w):
     """Time every kernel variant built for the workload's head dim and
     dtype (the default first), `args.sweep_reps` rounds with the order
-    reversed every other round; print a Markdown table of medians."""
+    reversed every other round, each measurement after `args.sweep_idle`
+    seconds idle so that all start from the same power state (30 launches
+    by default: a burst below the board's power limit); print a Markdown
+    table of medians."""
     import torch
 
     import exact_attention_forward_07_gb300 as fa
@@ -556,7 +559,7 @@ def run_sweep(args, w):
     if w.causal:  # the default kernel under each causal item order
         cands += [dict(cands[0], causal_order=o) for o in (-1, 0)]
     stream = torch.cuda.current_stream(dev)
-    steps = args.steps or 100
+    steps = args.steps or 30
     sampler = ClockSampler.for_device(dev.index)
     sampler.start()
     results = {i: [] for i in range(len(cands))}
@@ -566,6 +569,7 @@ def run_sweep(args, w):
             order.reverse()
         for i in order:
             kw = cands[i]
+            time.sleep(args.sweep_idle)  # every entry starts from the same idle power state
             for _ in range(args.warmup):
                 fa.fa_fwd_variant(q, k, v, o, lse, causal=w.causal, stream=stream, **kw)
             torch.cuda.synchronize(dev)
@@ -648,7 +652,9 @@ def main(argv=None):
     ap.add_argument("--variant", default="",
                     help="kernel variant, e.g. stages=3,exp_split=4 (fa_fwd_variant)")
     ap.add_argument("--sweep", action="store_true", help="time every built variant")
-    ap.add_argument("--sweep-reps", type=int, default=3)
+    ap.add_argument("--sweep-reps", type=int, default=5)
+    ap.add_argument("--sweep-idle", type=float, default=0.5,
+                    help="seconds idle before each sweep measurement")
     ap.add_argument("--rescale-stats", action="store_true",
                     help="count the O rescales of the workload (counting build)")
     ap.add_argument("--no-e2e", action="store_true")
