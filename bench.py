@@ -40,6 +40,11 @@ rate, which removes the power limit's effect on the clock).
 `--rescale-stats` runs the counting build once and prints how often the
 online softmax's O rescale fired.
 
+`--pass bwd` times the backward pass instead (fa_bwd: dQ, dK, dV from the
+forward's O and LSE and a seeded output gradient, three kernels per step;
+10*B*H*N^2*d FLOPs per step, halved when causal: the five matrix products
+of the gradients), with the backward oracle as its CPU baseline.
+
 `--impl reference` times the CPU oracle (the reference arm: a plain fp64
 C implementation of the definition) on the host cores, each step a bounded
 sample of the same workload (128 query rows of one head).
@@ -63,6 +68,7 @@ if ROOT not in sys.path:
 from attn_inputs import WORKLOADS, make_workload_inputs  # noqa: E402
 
 METRIC = "attention fwd TFLOPS (bf16, 1×GB300) and fraction of dense tensor-core peak"
+METRIC_BWD = "attention bwd TFLOPS (bf16, 1×GB300) and fraction of dense tensor-core peak"
 DEFAULT_WORKLOAD = "b1h32n16384d128_causal"
 FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCES = ["fa_api.cu", "fa_kernel.cuh", "ptx.cuh"]
@@ -316,6 +322,33 @@ def oracle_sample(w, q, k, v, n_heads: int, rows_per_head=None):
     return flops / dt / 1e12, dt, desc
 
 
+def bwd_output_grad(w):
+    """The output gradient of the backward benchmark: N(0,1) from its own
+    seeded generator, in the workload's 16-bit type."""
+    import torch
+    g = torch.Generator(device="cpu")
+    g.manual_seed(10 * w.index + 7)
+    return torch.randn((w.B, w.H, w.N, w.d), generator=g, dtype=torch.float32).to(
+        w.torch_dtype)
+
+
+def oracle_bwd_sample(w, q, k, v, do, n_heads: int):
+    """Time the backward oracle on the first `n_heads` heads (every row).
+    Returns (TFLOPS at the metric's 10*N^2*d per head, seconds, description)."""
+    import oracle
+    BH = w.B * w.H
+    heads = min(n_heads, BH)
+    sub = [oracle._as_f64(x.reshape(BH, 1, w.N, w.d)[:heads].reshape(1, heads, w.N, w.d))
+           for x in (q, k, v, do)]
+    t0 = time.perf_counter()
+    oracle.attn_bwd(*sub, w.causal, w.scale, nthreads=cpu_cores())
+    dt = time.perf_counter() - t0
+    flops = 10.0 * heads * w.N * w.N * w.d / (2 if w.causal else 1)
+    desc = (f"backward of {heads} head(s) x all rows of {w.name}, fp64, "
+            f"{min(heads, cpu_cores())} threads (one per head)")
+    return flops / dt / 1e12, dt, desc
+
+
 def run_reference(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -393,6 +426,19 @@ def run_ours(args, w):
             fa.fa_fwd_variant(q, k, v, o, lse, causal=causal, stream=stream, **variant)
     stream = torch.cuda.current_stream(dev)
     flops = w.flops()
+    bwd = args.pass_ == "bwd"
+    if bwd:
+        # the forward once (untimed) for O and LSE; each step is fa_bwd
+        o_f, lse_f = fa.forward(q, k, v, causal=w.causal, stream=stream)
+        do_h = bwd_output_grad(w)
+        do = do_h.to(dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(fa.fa_bwd_workspace_size(w.B, w.H, w.N, w.d), dtype=torch.uint8,
+                         device=dev)
+
+        def call(q, k, v, o, lse, causal, stream):  # noqa: F811
+            fa.fa_bwd(q, k, v, o_f, lse_f, do, dq, dk, dv, ws, causal=causal, stream=stream)
+        flops = 2.5 * w.flops()
 
     w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for i in range(args.warmup):
@@ -443,7 +489,7 @@ def run_ours(args, w):
     # overlapping the forward of another.  Timed on the host clock around
     # fully synchronised steps.
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not bwd:
         pin = [x.pin_memory() for x in (q_h, k_h, v_h)]
         o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
         lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
@@ -491,7 +537,10 @@ def run_ours(args, w):
                 "peak_source": peak_kind + (" (timed region >= 1 s)" if sustained else
                                             " (timed region < 1 s)"),
                 "traffic": profiled_traffic(w.name),
-                "kernel": "fa_fwd_kernel<%d,%s>" % (w.d, "bf16" if w.dtype == "bf16" else "fp16")}
+                "kernel": "%s<%d,%s>" % ("fa_bwd_kernel" if bwd else "fa_fwd_kernel", w.d,
+                                         "bf16" if w.dtype == "bf16" else "fp16")}
+    if bwd:  # no committed ncu summary of the backward is tied to this number
+        roofline["traffic"] = profiled_traffic("bwd_" + w.name)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -499,18 +548,23 @@ def run_ours(args, w):
         n_heads = int(args.cpu_heads)
         if n_heads <= 0:  # about CPU_SAMPLE_FLOP of oracle work: whole heads
             n_heads = max(1, round(CPU_SAMPLE_FLOP / (flops / (w.B * w.H))))
-        tf, dt, desc = oracle_sample(w, *q64, n_heads=n_heads)
+        if bwd:
+            tf, dt, desc = oracle_bwd_sample(w, *q64, do_h, n_heads=max(1, n_heads // 2))
+        else:
+            tf, dt, desc = oracle_sample(w, *q64, n_heads=n_heads)
         cpu = {"value": tf, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
                "sample": desc, "seconds": dt}
 
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic",
         "config": dict(w.describe(), parallelism=f"replicas{world}" if world > 1 else "single",
-                       l2=l2_note(w), **({"variant": variant} if variant else {})),
-        "gpu_launches": args.steps,
+                       l2=l2_note(w), **({"variant": variant} if variant else {}),
+                       **({"pass": "bwd"} if bwd else {})),
+        "gpu_launches": args.steps * (3 if bwd else 1),
         "clocks": clocks,
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -649,6 +703,8 @@ def main(argv=None):
     ap.add_argument("--e2e-chunks", type=int, default=8)
     ap.add_argument("--cpu-heads", type=int, default=0,
                     help="heads in the cpu_baseline sample (0: about 1.1e12 FLOP of them)")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="time the forward (default) or the backward")
     ap.add_argument("--variant", default="",
                     help="kernel variant, e.g. stages=3,exp_split=4 (fa_fwd_variant)")
     ap.add_argument("--sweep", action="store_true", help="time every built variant")

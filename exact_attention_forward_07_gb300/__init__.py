@@ -17,8 +17,8 @@ import math
 import os
 
 __all__ = ["FaError", "fa_fwd_host", "fa_fwd_noalloc", "fa_fwd", "fa_fwd_fp16", "fa_fwd_ex",
-           "fa_fwd_variant", "fa_get_status", "fa_strerror", "fa_version", "forward",
-           "library_path", "lib", "variants"]
+           "fa_fwd_variant", "fa_bwd", "fa_bwd_workspace_size", "fa_get_status", "fa_strerror",
+           "fa_version", "forward", "backward", "library_path", "lib", "variants"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
@@ -36,6 +36,8 @@ FA_ERR_TIMEOUT = -9
 FA_ERR_ALIAS = -10
 FA_ERR_OPTION = -11
 FA_ERR_SCRATCH = -12
+FA_ERR_WORKSPACE = -13
+FA_ERR_INTERNAL = -14
 FA_MAX_N = 1 << 20
 FA_NOALLOC_SCRATCH_BYTES = 16 << 20
 FA_HOST_DEFAULT_CHUNKS = 8
@@ -83,6 +85,11 @@ def lib():
                                      ctypes.c_float, ctypes.c_int, ctypes.c_float, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_int, P, P]
         L.fa_fwd_variant.restype = ctypes.c_int
+        L.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, I64, I64, I64, I64,
+                             ctypes.c_int, ctypes.c_float, ctypes.c_int, P]
+        L.fa_bwd.restype = ctypes.c_int
+        L.fa_bwd_workspace_size.argtypes = [I64, I64, I64, I64, ctypes.POINTER(ctypes.c_size_t)]
+        L.fa_bwd_workspace_size.restype = ctypes.c_int
         L.fa_variant_count.argtypes = []
         L.fa_variant_count.restype = ctypes.c_int
         IP = ctypes.POINTER(ctypes.c_int)
@@ -216,6 +223,54 @@ def fa_fwd_variant(q, k, v, o, lse, causal=False, scale=None, rescale_threshold=
     _call("fa_fwd_variant", q, k, v, o, lse, causal, scale, stream, q.dtype,
           extra=(fp16, float(rescale_threshold), int(stages), int(exp_split),
                  int(causal_order), sp))
+
+
+def fa_bwd_workspace_size(B, H, N, d) -> int:
+    """Bytes of device workspace fa_bwd needs for [B, H, N, d]."""
+    n = ctypes.c_size_t(0)
+    rc = lib().fa_bwd_workspace_size(int(B), int(H), int(N), int(d), ctypes.byref(n))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_workspace_size")
+    return n.value
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, causal=False, scale=None,
+           stream=None) -> None:
+    """Attention backward into caller-provided dq, dk, dv [B,H,N,d] (dtype of
+    q) from the forward's q, k, v, o, lse and the output gradient dout;
+    `workspace` is a CUDA uint8 tensor of at least fa_bwd_workspace_size
+    bytes (256-byte aligned, as torch allocates)."""
+    import torch
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"unsupported dtype {q.dtype}: use bfloat16 or float16")
+    B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq),
+                    ("dk", dk), ("dv", dv)):
+        _check(t, name, q.dtype, (B, H, N, d))
+    _check(lse, "lse", torch.float32, (B, H, N))
+    if not (isinstance(workspace, torch.Tensor) and workspace.is_cuda and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc = lib().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                      dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                      workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                      B, H, N, d, int(bool(causal)), float(scale), int(q.dtype == torch.float16),
+                      _stream_handle(stream, q.device))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd")
+
+
+def backward(q, k, v, o, lse, dout, causal=False, scale=None, stream=None):
+    """Allocate dq, dk, dv and the workspace with torch and run the backward;
+    returns (dq, dk, dv)."""
+    import torch
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa_bwd_workspace_size(*q.shape), dtype=torch.uint8, device=q.device)
+    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, ws, causal, scale, stream)
+    return dq, dk, dv
 
 
 def variants():

@@ -12,6 +12,7 @@
 #include <vector>
 
 #include "fa.h"
+#include "fa_bwd_kernel.cuh"
 #include "fa_kernel.cuh"
 
 namespace {
@@ -49,6 +50,8 @@ struct DeviceState {
   size_t stage_bytes = 0;
   std::once_flag attr_once[kMaxVariants];  // shared-memory attribute, per kernel variant
   int attr_err[kMaxVariants] = {};
+  std::once_flag bwd_attr_once[4];  // backward kernels: [d == 128][fp16]
+  int bwd_attr_err[4] = {};
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -488,6 +491,84 @@ int fwd_common(bool bf16, const void *q, const void *k, const void *v, void *o, 
                                stats, order, static_cast<cudaStream_t>(stream));
 }
 
+// ------------------------------------------------------------- backward
+// Workspace of the backward: lse * log2(e) and D = rowsum(dO * O) per row,
+// then the fp32 dQ accumulators, rows padded to whole 128-row tiles.
+struct BwdWorkspace {
+  size_t lse2 = 0, dd = 0, acc = 0, total = 0;  // byte offsets and size
+};
+
+BwdWorkspace bwd_workspace(int64_t BH, int64_t N, int64_t d) {
+  const int64_t Np = (N + 127) / 128 * 128;
+  BwdWorkspace w;
+  w.lse2 = 0;
+  w.dd = static_cast<size_t>(BH * Np) * 4;
+  w.acc = w.dd + static_cast<size_t>(BH * Np) * 4;
+  w.total = w.acc + static_cast<size_t>(BH * Np * d) * 4;
+  return w;
+}
+
+int bwd_shape_check(int64_t B, int64_t H, int64_t N, int64_t d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (N > FA_MAX_N) return FA_ERR_UNSUPPORTED_N;
+  const int64_t kLimit = int64_t(1) << 40;
+  if (B > kLimit / H || B * H > kLimit / N || B * H * N > kLimit / d) return FA_ERR_SHAPE;
+  if (B * H * ((N + 127) / 128) > INT32_MAX / 2) return FA_ERR_SHAPE;
+  return FA_OK;
+}
+
+template <int D, bool BF16>
+int launch_bwd(DeviceState &ds, const void *q, const void *k, const void *v, const void *o,
+               const float *lse, const void *dout, void *dq, void *dk, void *dv,
+               uint8_t *ws, int64_t BH, int64_t N, int causal, float scale, cudaStream_t stream) {
+  using C = fa::BwdCfg<D, BF16>;
+  auto kernel = fa::fa_bwd_kernel<D, BF16>;
+  const int slot = (D == 128 ? 2 : 0) + (BF16 ? 0 : 1);
+  std::call_once(ds.bwd_attr_once[slot], [&] {
+    ds.bwd_attr_err[slot] = static_cast<int>(
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+  });
+  if (ds.bwd_attr_err[slot] != 0) return cuda_fail(static_cast<cudaError_t>(ds.bwd_attr_err[slot]));
+  CUtensorMap tq, tk, tv, tdo;
+  int rc;
+  if ((rc = make_map(&tq, q, BF16, BH, N, D)) != FA_OK) return rc;
+  if ((rc = make_map(&tk, k, BF16, BH, N, D)) != FA_OK) return rc;
+  if ((rc = make_map(&tv, v, BF16, BH, N, D)) != FA_OK) return rc;
+  if ((rc = make_map(&tdo, dout, BF16, BH, N, D)) != FA_OK) return rc;
+  const BwdWorkspace w = bwd_workspace(BH, N, D);
+  fa::BwdParams p;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.lse2 = reinterpret_cast<float *>(ws + w.lse2);
+  p.dd = reinterpret_cast<float *>(ws + w.dd);
+  p.dq_acc = reinterpret_cast<float4 *>(ws + w.acc);
+  p.status = ds.status;
+  p.N = static_cast<int>(N);
+  p.n_tiles = static_cast<int>((N + 127) / 128);
+  p.Np = p.n_tiles * 128;
+  p.BH = static_cast<int>(BH);
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  const dim3 tiles(static_cast<unsigned>(p.n_tiles), static_cast<unsigned>(BH));
+  fa::fa_bwd_prep_kernel<D, BF16><<<tiles, 256, 0, stream>>>(p);
+  kernel<<<static_cast<unsigned>(BH * p.n_tiles), C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv,
+                                                                                         tdo, p);
+  fa::fa_bwd_dq_kernel<D, BF16><<<tiles, 128, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
+      return FA_ERR_DEVICE;
+    return cuda_fail(e);
+  }
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -529,6 +610,57 @@ int fa_fwd_variant(const void *q, const void *k, const void *v, void *o, float *
   if (stats != nullptr && (reinterpret_cast<uintptr_t>(stats) & 7u)) return FA_ERR_ALIGN;
   return fwd_common(fp16 == 0, q, k, v, o, lse, B, H, N, d, causal, scale, rescale_threshold,
                     stream, /*noalloc=*/false, idx, stats, causal_order);
+}
+
+int fa_bwd_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d, size_t *bytes) {
+  if (!bytes) return FA_ERR_NULL;
+  const int rc = bwd_shape_check(B, H, N, d);
+  if (rc != FA_OK) return rc;
+  *bytes = bwd_workspace(B * H, N, d).total;
+  return FA_OK;
+}
+
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+           const void *dout, void *dq, void *dk, void *dv, void *workspace,
+           size_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t d, int causal,
+           float scale, int fp16, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace)
+    return FA_ERR_NULL;
+  int rc = bwd_shape_check(B, H, N, d);
+  if (rc != FA_OK) return rc;
+  if (B * H > 65535) return FA_ERR_SHAPE;  // grid y of the row kernels
+  for (const void *ptr : {q, k, v, o, dout, static_cast<const void *>(dq),
+                          static_cast<const void *>(dk), static_cast<const void *>(dv)})
+    if (reinterpret_cast<uintptr_t>(ptr) & 15u) return FA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGN;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+  const int64_t BH = B * H;
+  const BwdWorkspace w = bwd_workspace(BH, N, d);
+  if (workspace_bytes < w.total) return FA_ERR_WORKSPACE;
+  const size_t tb = static_cast<size_t>(BH * N * d) * 2, lb = static_cast<size_t>(BH * N) * 4;
+  const void *outs[3] = {dq, dk, dv};
+  for (int a = 0; a < 3; ++a) {
+    for (const void *in : {q, k, v, o, dout})
+      if (overlaps(outs[a], tb, in, tb)) return FA_ERR_ALIAS;
+    if (overlaps(outs[a], tb, lse, lb) || overlaps(outs[a], tb, workspace, w.total))
+      return FA_ERR_ALIAS;
+    for (int b = a + 1; b < 3; ++b)
+      if (overlaps(outs[a], tb, outs[b], tb)) return FA_ERR_ALIAS;
+  }
+  for (const void *in : {q, k, v, o, dout})
+    if (overlaps(workspace, w.total, in, tb)) return FA_ERR_ALIAS;
+  if (overlaps(workspace, w.total, lse, lb)) return FA_ERR_ALIAS;
+
+  DeviceState *ds = nullptr;
+  rc = device_state(&ds);
+  if (rc != FA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+#define FA_BWD(DD, BB) launch_bwd<DD, BB>(*ds, q, k, v, o, lse, dout, dq, dk, dv, ws, BH, N, causal, scale, st)
+  if (d == 64) return fp16 ? FA_BWD(64, false) : FA_BWD(64, true);
+  return fp16 ? FA_BWD(128, false) : FA_BWD(128, true);
+#undef FA_BWD
 }
 
 int fa_variant_count(void) { return kNumVariants; }
@@ -694,7 +826,8 @@ int fa_get_status(fa_stream_t stream) {
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  return (v & fa::kStatusTimeout) ? FA_ERR_TIMEOUT : FA_OK;
+  if (v & fa::kStatusTimeout) return FA_ERR_TIMEOUT;
+  return (v & fa::kStatusLayout) ? FA_ERR_INTERNAL : FA_OK;
 }
 
 const char *fa_strerror(int code) {
@@ -715,6 +848,9 @@ const char *fa_strerror(int code) {
              "self-test limit in [1, 1e6] us)";
     case FA_ERR_SCRATCH:
       return "fa_fwd_noalloc: the split schedule needs more than FA_NOALLOC_SCRATCH_BYTES";
+    case FA_ERR_WORKSPACE: return "fa_bwd: workspace smaller than fa_bwd_workspace_size";
+    case FA_ERR_INTERNAL:
+      return "a kernel found its shared memory base unaligned and did no work; outputs undefined";
     default: return "unknown error code";
   }
 }

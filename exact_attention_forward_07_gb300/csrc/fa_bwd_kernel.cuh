@@ -1,0 +1,470 @@
+// fa_bwd_kernel.cuh -- the attention backward for sm_103a.
+//
+// Gradients of L = sum(dO * O) for the attention forward O = softmax(scale
+// Q K^T [+ causal mask]) V, from the forward's O and logsumexp (the
+// FlashAttention v4 Blackwell pipeline diagram names the backward pass in
+// its pseudo-code panel, "backward idea", and its CTA-role panel: the
+// backward accumulates dQ with atomic additions, which larger MMA tiles
+// reduce).  With P recomputed from the logsumexp, per (query i, key j):
+//
+//   P  = exp(scale q_i.k_j - lse_i)           dV_j += P dO_i
+//   dP = dO_i . v_j                           dS    = P (dP - D_i)
+//   D_i = dO_i . O_i                          dQ_i += scale dS k_j
+//                                             dK_j += scale dS q_i
+//
+// D_i = rowsum(dO * O) equals rowsum(P * dP) because O_i = sum_j P_ij v_j.
+//
+// Three kernels:
+//   fa_bwd_prep_kernel   D and lse * log2(e) per row (padded to whole
+//                        128-row tiles), and the dQ accumulators zeroed
+//   fa_bwd_kernel        one CTA per (head, 128-key block j): K_j and V_j
+//                        stay in shared memory while the CTA walks the
+//                        query blocks i (causal: i >= j) through a two-stage
+//                        TMA ring of Q_i and dO_i; five tcgen05 MMAs per step
+//   fa_bwd_dq_kernel     dQ = scale * accumulators, rounded to 16 bits
+//
+// Roles in fa_bwd_kernel (512 threads):
+//   warp  0     TMA producer (one thread)
+//   warp  1     MMA issue (one elected lane) + tensor-memory allocation
+//   warps 4-11  dS warps: warp w owns the keys of lane quadrant w % 4 (one
+//               thread per key) and half of the query columns; they form
+//               P^T and dS^T, then write the block's dK and dV
+//   warps 12-15 dQ warps: read each step's dQ out of tensor memory (one
+//               thread per query row) and add it to the fp32 accumulators
+//
+// Per step (query block i):
+//   S^T  = K_j Q_i^T      SS  -> TMEM [0,128)     (lanes = keys)
+//   dP^T = V_j dO_i^T     SS  -> TMEM [128,256)
+//   dS warps: P^T = 2^(S^T scale log2e - lse2_i), packed to 16 bits over
+//   S^T; dS^T = P^T (dP^T - D_i) to shared memory, 128-byte swizzled
+//   dV  += P^T dO_i       TS  (P^T from TMEM, dO_i MN-major)
+//   dK  += dS^T Q_i       SS  (dS^T K-major, Q_i MN-major)
+//   dQ_i = dS K_j         SS  (the same dS buffer read MN-major, K_j MN-major)
+// The dS buffer [query half][128 key rows][128 bytes] is at once the
+// K-major layout of dS^T (rows = keys) and the MN-major layout of dS (64
+// queries per swizzled row, keys along the rows), so one store serves both
+// MMAs.  dQ goes to the columns of dP^T at d = 128 (tensor memory is full:
+// S, dP, dK and dV take 512 columns), so the next dP^T waits until the dQ
+// warps have read it; at d = 64 it has columns of its own.
+//
+// Every wait is bounded as in the forward kernel; a wait that gives up sets
+// the abort flag and the status word, in-flight copies and MMAs are drained
+// and tensor memory is freed before the CTA exits.
+#pragma once
+
+#include "fa_kernel.cuh"
+
+namespace fa {
+
+constexpr uint32_t kStatusLayout = 2u;  // shared-memory base not 1024-byte aligned
+
+struct BwdParams {
+  const void *o;      // [BH, N, D] 16-bit forward output
+  const void *dout;   // [BH, N, D] 16-bit
+  const float *lse;   // [BH, N] natural-log logsumexp of the forward
+  void *dq, *dk, *dv; // [BH, N, D] 16-bit
+  float *lse2;        // [BH, Np]: lse * log2(e); +inf past N
+  float *dd;          // [BH, Np]: rowsum(dO * O); 0 past N
+  float4 *dq_acc;     // [BH][Np / 128][D / 4][128] fp32 x 4
+  unsigned *status;
+  int N, Np, BH;
+  int n_tiles;        // Np / 128
+  int causal;
+  float scale;
+  float scale_log2;   // scale * log2(e)
+};
+
+template <int D, bool BF16>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
+  static constexpr int kTile = 128 * D * 2;   // one 128-row tile of 16-bit elements
+  static constexpr int kHalf = 128 * 64 * 2;  // 64 columns of 128 rows: one swizzle span
+  static constexpr int kK = 0, kV = kTile;
+  static constexpr int kQ = 2 * kTile;        // two stages
+  static constexpr int kDO = kQ + 2 * kTile;  // two stages
+  static constexpr int kDS = kDO + 2 * kTile; // dS^T, [query half][128 key rows][128 bytes]
+  static constexpr int kLse = kDS + 2 * kHalf;  // [stage][128] fp32
+  static constexpr int kDd = kLse + 2 * 512;    // [stage][128] fp32
+  static constexpr int kBar = kDd + 2 * 512;
+  // barriers: K/V loaded; Q/dO stage full (2) and empty (2); S^T and dP^T
+  // done; dS written (8 arrivals); dQ done; dQ read (4 arrivals); dK/dV done;
+  // drain
+  static constexpr int bKV = 0, bFull = 1, bEmpty = 3, bSdp = 5, bDs = 6, bDqFull = 7,
+                       bDqFree = 8, bDkdv = 9, bDrain = 10, kNumBars = 11;
+  static constexpr int kMisc = kBar + kNumBars * 8;  // tmem base, abort flag
+  static constexpr int kUsed = kMisc + 16;
+  // 1 KiB of slack for the 1024-byte alignment of the tiles when it fits in
+  // the 227 KiB a CTA may use; at d = 128 only 920 bytes fit, and the kernel
+  // checks that the base it gets leaves room (it does when the dynamic
+  // shared memory starts 1024-aligned)
+  static constexpr int kMaxSmem = 227 * 1024;
+  static constexpr int kSmemBytes = kUsed + 1024 < kMaxSmem ? kUsed + 1024 : kMaxSmem;
+  static_assert(kUsed <= kMaxSmem, "shared memory beyond the per-CTA limit");
+  static constexpr bool kDqAliasDp = (D == 128);
+  static constexpr uint32_t cS = 0, cDP = 128, cDK = 256, cDV = 256 + D;
+  static constexpr uint32_t cDQ = kDqAliasDp ? cDP : 256 + 2 * D;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kIdescS = idesc_f16(BF16, false, 128, 128);         // S^T, dP^T
+  static constexpr uint32_t kIdescG = idesc_f16(BF16, true, 128, D);            // dV, dK
+  static constexpr uint32_t kIdescQ = idesc_f16_ab(BF16, true, true, 128, D);   // dQ
+  static constexpr int kThreads = 512;
+};
+
+// D and lse * log2(e) for one 128-row tile of one head, and that tile's
+// dQ accumulators zeroed.  256 threads; warp w takes rows 16w..16w+15, its
+// lanes splitting each row's D columns.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdParams p) {
+  const int tile = blockIdx.x, bh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kPer = D / 32;  // elements per lane: 4 (d = 128) or 2 (d = 64)
+  for (int r = 16 * warp; r < 16 * warp + 16; ++r) {
+    const int n = tile * 128 + r;
+    float dot = 0.f;
+    if (n < p.N) {
+      const size_t off = (static_cast<size_t>(bh) * p.N + n) * D + lane * kPer;
+      const uint16_t *po = static_cast<const uint16_t *>(p.o) + off;
+      const uint16_t *pd = static_cast<const uint16_t *>(p.dout) + off;
+      uint16_t a[kPer], b[kPer];
+      if constexpr (kPer == 4) {
+        *reinterpret_cast<uint2 *>(a) = *reinterpret_cast<const uint2 *>(po);
+        *reinterpret_cast<uint2 *>(b) = *reinterpret_cast<const uint2 *>(pd);
+      } else {
+        *reinterpret_cast<uint32_t *>(a) = *reinterpret_cast<const uint32_t *>(po);
+        *reinterpret_cast<uint32_t *>(b) = *reinterpret_cast<const uint32_t *>(pd);
+      }
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) {
+        float x, y;
+        if constexpr (BF16) {
+          x = __bfloat162float(__ushort_as_bfloat16(a[e]));
+          y = __bfloat162float(__ushort_as_bfloat16(b[e]));
+        } else {
+          x = __half2float(__ushort_as_half(a[e]));
+          y = __half2float(__ushort_as_half(b[e]));
+        }
+        dot = fmaf(x, y, dot);
+      }
+#pragma unroll
+      for (int sh = 16; sh >= 1; sh >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, sh);
+    }
+    if (lane == 0) {
+      const size_t row = static_cast<size_t>(bh) * p.Np + n;
+      p.dd[row] = n < p.N ? dot : 0.f;
+      p.lse2[row] = n < p.N ? p.lse[static_cast<size_t>(bh) * p.N + n] * 1.4426950408889634f
+                            : INFINITY;
+    }
+  }
+  float4 *acc = p.dq_acc + (static_cast<size_t>(bh) * p.n_tiles + tile) * (D / 4) * 128;
+  for (int i = threadIdx.x; i < (D / 4) * 128; i += 256) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// dQ = scale * accumulators, rounded to 16 bits: one 128-row tile of one
+// head; thread = row, 32 columns at a time, stored through the in-warp
+// transpose so each store instruction writes whole 64-byte row segments.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(128) fa_bwd_dq_kernel(const BwdParams p) {
+  const int tile = blockIdx.x, bh = blockIdx.y;
+  const uint32_t lane = threadIdx.x & 31;
+  const int row = threadIdx.x;
+  const int n = tile * 128 + row;
+  const float4 *acc =
+      p.dq_acc + (static_cast<size_t>(bh) * p.n_tiles + tile) * (D / 4) * 128 + row;
+  uint8_t *row0 = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.dq) +
+                                              (static_cast<size_t>(bh) * p.N + n - lane) * D);
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint4 v4[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float4 x = acc[(8 * c + 2 * u) * 128], y = acc[(8 * c + 2 * u + 1) * 128];
+      v4[u] = make_uint4(pack2<BF16>(x.x * p.scale, x.y * p.scale),
+                         pack2<BF16>(x.z * p.scale, x.w * p.scale),
+                         pack2<BF16>(y.x * p.scale, y.y * p.scale),
+                         pack2<BF16>(y.z * p.scale, y.w * p.scale));
+    }
+    store_rows<4>(v4, row0 + 64 * c, static_cast<size_t>(D) * 2, p.N - (n - static_cast<int>(lane)),
+                  lane);
+  }
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const BwdParams p) {
+  using C = BwdCfg<D, BF16>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  if (sbase - raw + C::kUsed > static_cast<uint32_t>(C::kSmemBytes)) {
+    // the tiles would not fit after alignment: every thread leaves at once
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusLayout);
+    return;
+  }
+  uint8_t *smem = smem_raw + (sbase - raw);
+  const uint32_t bars = sbase + C::kBar;
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+  uint32_t *tmem_base_slot = reinterpret_cast<uint32_t *>(smem + C::kMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31u;
+  // this CTA's key block; the CTAs of one head are consecutive, heaviest
+  // (causal: the first key block sees every query block) first
+  const int T = p.n_tiles;
+  const int bh = blockIdx.x / T;
+  const int jb = blockIdx.x - bh * T;
+  const int i0 = p.causal ? jb : 0;
+  const int n_steps = T - i0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::bKV), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::bFull + s), 1);
+      mbar_init(bar(C::bEmpty + s), 1);
+    }
+    mbar_init(bar(C::bSdp), 1);
+    mbar_init(bar(C::bDs), 8);      // one arrival per dS warp
+    mbar_init(bar(C::bDqFull), 1);
+    mbar_init(bar(C::bDqFree), 4);  // one arrival per dQ warp
+    mbar_init(bar(C::bDkdv), 1);
+    mbar_init(bar(C::bDrain), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_do);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_base_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_once = l2_policy_evict_first();  // K_j, V_j: read by this CTA only
+      const uint64_t pol_reuse = l2_policy_evict_last();  // Q_i, dO_i: read by every CTA of the head
+      mbar_arrive_expect_tx(bar(C::bKV), 2 * C::kTile);
+      for (int h = 0; h < D / 64; ++h) {
+        tma_load_3d(sbase + C::kK + h * C::kHalf, &tm_k, bar(C::bKV), h * 64, jb * 128, bh, pol_once);
+        tma_load_3d(sbase + C::kV + h * C::kHalf, &tm_v, bar(C::bKV), h * 64, jb * 128, bh, pol_once);
+      }
+      int issued = 0;
+      for (int t = 0; t < n_steps; ++t) {
+        const int s = t & 1;
+        if (t >= 2 && !wait_bar(bar(C::bEmpty + s), ((t >> 1) + 1) & 1u, abort_flag, p.status)) break;
+        const int i = i0 + t;
+        mbar_arrive_expect_tx(bar(C::bFull + s), 2 * C::kTile + 1024);
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_3d(sbase + C::kQ + s * C::kTile + h * C::kHalf, &tm_q, bar(C::bFull + s), h * 64,
+                      i * 128, bh, pol_reuse);
+          tma_load_3d(sbase + C::kDO + s * C::kTile + h * C::kHalf, &tm_do, bar(C::bFull + s),
+                      h * 64, i * 128, bh, pol_reuse);
+        }
+        const size_t row = static_cast<size_t>(bh) * p.Np + static_cast<size_t>(i) * 128;
+        bulk_load(sbase + C::kLse + s * 512, p.lse2 + row, 512, bar(C::bFull + s));
+        bulk_load(sbase + C::kDd + s * 512, p.dd + row, 512, bar(C::bFull + s));
+        ++issued;
+      }
+      // drain: every issued copy lands before shared memory is released
+      wait_drain(bar(C::bKV), 0, abort_flag, p.status);
+      for (int s = 0; s < 2; ++s) {
+        const int cnt = (issued - s + 1) / 2;  // loads into stage s
+        if (cnt > 0) wait_drain(bar(C::bFull + s), (cnt - 1) & 1u, abort_flag, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issue
+    const uint32_t leader = elect_one();
+    const uint64_t kdesc0 = smem_desc_sw128(0, 16, 1024);       // K-major tiles
+    const uint64_t mdesc0 = smem_desc_sw128(0, C::kHalf, 1024); // MN-major tiles
+    // D[tmem] (+)= A B over a K extent of 16 * ksteps, A and B K-major tiles
+    // of 64-column halves (the layout TMA writes)
+    auto ss_kk = [&](uint32_t dcol, uint32_t a, uint32_t b, uint32_t idesc, int ksteps,
+                     bool acc) {
+      const uint64_t ad = kdesc0 + (a >> 4), bd = kdesc0 + (b >> 4);
+      for (int kk = 0; kk < ksteps; ++kk) {
+        const uint32_t off = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;
+        mma_ss_if(leader, tmem + dcol, ad + off, bd + off, idesc, (acc || kk > 0) ? 1u : 0u);
+      }
+    };
+    bool ok = wait_bar(bar(C::bKV), 0, abort_flag, p.status);
+    for (int t = 0; ok && t < n_steps; ++t) {
+      const int s = t & 1;
+      const uint32_t q_s = sbase + C::kQ + s * C::kTile, do_s = sbase + C::kDO + s * C::kTile;
+      if (!(ok = wait_bar(bar(C::bFull + s), (t >> 1) & 1u, abort_flag, p.status))) break;
+      tc_fence_after();
+      ss_kk(C::cS, sbase + C::kK, q_s, C::kIdescS, D / 16, false);     // S^T = K Q^T
+      if (C::kDqAliasDp && t > 0) {  // dQ(t-1) read out of the dP columns
+        if (!(ok = wait_bar(bar(C::bDqFree), (t - 1) & 1u, abort_flag, p.status))) break;
+        tc_fence_after();
+      }
+      ss_kk(C::cDP, sbase + C::kV, do_s, C::kIdescS, D / 16, false);   // dP^T = V dO^T
+      mma_commit_if(leader, bar(C::bSdp));
+      if (!(ok = wait_bar(bar(C::bDs), t & 1u, abort_flag, p.status))) break;
+      tc_fence_after();
+      // dV += P^T dO: P^T packed in tensor memory, half h of the queries at
+      // columns [64h, 64h + 32)
+      const uint64_t bdo = mdesc0 + (do_s >> 4), bq = mdesc0 + (q_s >> 4);
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts_if(leader, tmem + C::cDV, tmem + C::cS + 64 * (kk >> 2) + 8 * (kk & 3),
+                  bdo + kk * (2048 >> 4), C::kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
+      // dK += dS^T Q: dS^T K-major in shared memory, Q MN-major
+      const uint64_t ads = kdesc0 + ((sbase + C::kDS) >> 4);
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;
+        mma_ss_if(leader, tmem + C::cDK, ads + off, bq + kk * (2048 >> 4), C::kIdescG,
+                  (t > 0 || kk > 0) ? 1u : 0u);
+      }
+      if (!C::kDqAliasDp && t > 0) {  // dQ(t-1) read out of its own columns
+        if (!(ok = wait_bar(bar(C::bDqFree), (t - 1) & 1u, abort_flag, p.status))) break;
+        tc_fence_after();
+      }
+      // dQ = dS K: the same buffer read MN-major, K MN-major
+      const uint64_t adt = mdesc0 + ((sbase + C::kDS) >> 4), bk = mdesc0 + ((sbase + C::kK) >> 4);
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss_if(leader, tmem + C::cDQ, adt + kk * (2048 >> 4), bk + kk * (2048 >> 4), C::kIdescQ,
+                  kk > 0 ? 1u : 0u);
+      mma_commit_if(leader, bar(C::bDqFull));
+      mma_commit_if(leader, bar(C::bEmpty + s));
+    }
+    if (ok) mma_commit_if(leader, bar(C::bDkdv));
+    mma_commit_if(leader, bar(C::bDrain));
+    wait_drain(bar(C::bDrain), 0, abort_flag, p.status);
+  } else if (warp >= 4 && warp < 12) {
+    // -------------------------------------------------------------- dS warps
+    const int w = warp - 4;
+    const int qd = w & 3, hf = w >> 2;  // lane quadrant (keys), half of the query columns
+    const int row = qd * 32 + static_cast<int>(lane);  // key within the block
+    const bool key_dead = jb * 128 + row >= p.N;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(qd * 32) << 16);
+    const uint64_t sl2_2 = f2(p.scale_log2, p.scale_log2);
+    uint8_t *ds_row = smem + C::kDS + hf * C::kHalf + row * 128;
+    bool ok = true;
+    for (int t = 0; ok && t < n_steps; ++t) {
+      if (!(ok = wait_bar(bar(C::bSdp), t & 1u, abort_flag, p.status))) break;
+      tc_fence_after();
+      const int s = t & 1, i = i0 + t;
+      const float *lse2s = reinterpret_cast<const float *>(smem + C::kLse + s * 512);
+      const float *dds = reinterpret_cast<const float *>(smem + C::kDd + s * 512);
+      const bool diag = p.causal && i == jb;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int q0 = 64 * hf + 32 * c;  // first query column of this chunk
+        uint32_t sr[32], dr[32];
+        tmem_ld32(t_lane + C::cS + q0, sr);
+        tmem_ld32(t_lane + C::cDP + q0, dr);
+        tmem_ld_wait(sr);
+        tmem_ld_wait(dr);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 l4 = *reinterpret_cast<const float4 *>(lse2s + q0 + e);
+          const float4 d4 = *reinterpret_cast<const float4 *>(dds + q0 + e);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int u = 0; u < 4; u += 2) {
+            float x0, x1;
+            f2_split(ffma2(f2(__uint_as_float(sr[e + u]), __uint_as_float(sr[e + u + 1])), sl2_2,
+                           f2(-lv[u], -lv[u + 1])),
+                     x0, x1);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if (key_dead || (diag && row > q0 + e + u)) p0 = 0.f;
+            if (key_dead || (diag && row > q0 + e + u + 1)) p1 = 0.f;
+            float g0, g1;
+            f2_split(fmul2(f2(p0, p1), fadd2(f2(__uint_as_float(dr[e + u]), __uint_as_float(dr[e + u + 1])),
+                                             f2(-dv[u], -dv[u + 1]))),
+                     g0, g1);
+            pk[(e + u) >> 1] = pack2<BF16>(p0, p1);
+            dk[(e + u) >> 1] = pack2<BF16>(g0, g1);
+          }
+        }
+        // P^T of these 32 queries: 16 packed columns over this chunk's own S^T
+        tmem_st16(t_lane + C::cS + 64 * hf + 16 * c, pk);
+        // dS^T: 64 bytes of the key's 128-byte row in this half, chunks
+        // 4c..4c+3 at their 128-byte-swizzle positions
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int pos = (4 * c + u) ^ (row & 7);
+          *reinterpret_cast<uint4 *>(ds_row + 16 * pos) =
+              make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();  // dS^T stores visible to the tensor core
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::bDs));
+    }
+    // epilogue: dK (times scale) and dV of this warp's keys, half the columns
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) ok = wait_bar(bar(C::bDkdv), 0, abort_flag, p.status);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      const int key0 = jb * 128 + qd * 32;  // key of lane 0
+      const size_t off = (static_cast<size_t>(bh) * p.N + key0) * D + (D / 2) * hf;
+      for (int g = 0; g < 2; ++g) {
+        uint8_t *row0 = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(g ? p.dv : p.dk) + off);
+        const float mul = g ? 1.f : p.scale;
+        const uint32_t col = (g ? C::cDV : C::cDK) + (D / 2) * hf;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t r[32];
+          tmem_ld32(t_lane + col + 32 * c, r);
+          tmem_ld_wait(r);
+          uint4 v4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            v4[u] = make_uint4(pack2<BF16>(__uint_as_float(r[8 * u]) * mul, __uint_as_float(r[8 * u + 1]) * mul),
+                               pack2<BF16>(__uint_as_float(r[8 * u + 2]) * mul, __uint_as_float(r[8 * u + 3]) * mul),
+                               pack2<BF16>(__uint_as_float(r[8 * u + 4]) * mul, __uint_as_float(r[8 * u + 5]) * mul),
+                               pack2<BF16>(__uint_as_float(r[8 * u + 6]) * mul, __uint_as_float(r[8 * u + 7]) * mul));
+          store_rows<4>(v4, row0 + 64 * c, static_cast<size_t>(D) * 2, p.N - key0, lane);
+        }
+      }
+    }
+    tc_fence_before();
+  } else if (warp >= 12) {
+    // -------------------------------------------------------------- dQ warps
+    const int qd = warp & 3;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(qd * 32) << 16);
+    bool ok = true;
+    for (int t = 0; ok && t < n_steps; ++t) {
+      if (!(ok = wait_bar(bar(C::bDqFull), t & 1u, abort_flag, p.status))) break;
+      tc_fence_after();
+      const int i = i0 + t;
+      float4 *dst = p.dq_acc + (static_cast<size_t>(bh) * T + i) * (D / 4) * 128 + qd * 32 + lane;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(t_lane + C::cDQ + 32 * c, r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          red_add_v4(dst + (8 * c + u) * 128, __uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                     __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::bDqFree));
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace fa

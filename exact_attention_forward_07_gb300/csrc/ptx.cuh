@@ -296,6 +296,32 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool b_mn_major, uin
          ((b_mn_major ? 1u : 0u) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f16, with the majorness of both operands:
+// bit 15 = A MN-major (A transposed), bit 16 = B MN-major.
+__host__ __device__ constexpr uint32_t idesc_f16_ab(bool bf16, bool a_mn_major, bool b_mn_major,
+                                                    uint32_t M, uint32_t N) {
+  return idesc_f16(bf16, b_mn_major, M, N) | ((a_mn_major ? 1u : 0u) << 15);
+}
+
+// 1-D bulk copy global -> shared, completion signalled on `bar` as bytes.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Four fp32 additions to consecutive global addresses (16-byte aligned),
+// performed in L2 without returning a value.
+__device__ __forceinline__ void red_add_v4(float4 *addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
 // ------------------------------------------------------------ arithmetic
 // Three-input maximum (one instruction on sm_100 and later).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {

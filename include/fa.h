@@ -51,6 +51,7 @@
 #ifndef FA_GB300_H
 #define FA_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -74,6 +75,8 @@ typedef void *fa_stream_t;
 #define FA_ERR_ALIAS (-10)         /* an output overlaps an input or the other output */
 #define FA_ERR_OPTION (-11)        /* an option (rescale threshold, self-test limit) out of range */
 #define FA_ERR_SCRATCH (-12)       /* fa_fwd_noalloc: the call needs more than its fixed scratch */
+#define FA_ERR_WORKSPACE (-13)     /* fa_bwd: the workspace is smaller than fa_bwd_workspace_size */
+#define FA_ERR_INTERNAL (-14)      /* (fa_get_status) a kernel found its shared memory unusable */
 
 #define FA_MAX_N (1 << 20)         /* longest sequence accepted */
 
@@ -221,6 +224,50 @@ int fa_variant_info(int index, int *d, int *fp16, int *stages, int *exp_split, i
  * FA_ERR_SHAPE / FA_ERR_HEADDIM on bad arguments.  For tests and tuning.
  */
 int fa_causal_order(int64_t B, int64_t H, int64_t N, int64_t d, int sm_count);
+
+/*
+ * fa_bwd -- gradients of the attention forward (the backward pass).
+ *
+ * The FlashAttention v4 Blackwell pipeline diagram names the backward pass
+ * (pseudo-code panel, "backward idea"; CTA-role panel: the backward adds
+ * dQ up with atomic additions, which larger MMA tiles reduce).  Given the
+ * forward's inputs q, k, v, its outputs o and lse (from fa_fwd /
+ * fa_fwd_fp16 / fa_fwd_ex with the same causal and scale), and dout = dL/dO
+ * for some loss L, fa_bwd writes dq = dL/dQ, dk = dL/dK, dv = dL/dV:
+ *
+ *   P_ij = exp(scale q_i.k_j - lse_i)   (j visible to i; else 0)
+ *   dv_j = sum_i P_ij dout_i            D_i  = dout_i . o_i
+ *   dS_ij = P_ij (dout_i . v_j - D_i)
+ *   dq_i = scale sum_j dS_ij k_j        dk_j = scale sum_i dS_ij q_i
+ *
+ * P and dS are recomputed tile by tile and never stored; P and dS are
+ * rounded to the 16-bit input type for the tensor-core products, with fp32
+ * accumulation; dq is accumulated in fp32 in the workspace.
+ *
+ *   q, k, v, o, dout : [B,H,N,d] 16-bit (fp16 != 0: fp16, else bf16), read only
+ *   lse              : [B,H,N] fp32, read only
+ *   dq, dk, dv       : [B,H,N,d] 16-bit, written (round to nearest even)
+ *   workspace        : DEVICE memory of at least fa_bwd_workspace_size(B,H,N,d)
+ *                      bytes, 256-byte aligned, owned by the caller;
+ *                      overwritten (nothing needs to be cleared before the
+ *                      call, nothing is kept after it).  Calls that run at the
+ *                      same time need separate workspaces.
+ *   B*H              : at most 65535
+ * Layout, d, causal, scale, alignment (16 bytes; lse 4) and stream as for
+ * fa_fwd.  The library allocates no memory.  Errors: as fa_fwd, plus
+ * FA_ERR_WORKSPACE (too small) and FA_ERR_ALIAS when an output overlaps an
+ * input, another output or the workspace.  Nothing is launched on an
+ * argument error.  Three kernels run on `stream`.
+ */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+           const void *dout, void *dq, void *dk, void *dv, void *workspace,
+           size_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t d, int causal,
+           float scale, int fp16, fa_stream_t stream);
+
+/* fa_bwd_workspace_size -- bytes of workspace fa_bwd needs for [B,H,N,d]:
+ * B*H*Np*(4*d + 8) with Np = N rounded up to a multiple of 128.  Host only.
+ * FA_ERR_NULL / FA_ERR_SHAPE / FA_ERR_HEADDIM / FA_ERR_UNSUPPORTED_N. */
+int fa_bwd_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d, size_t *bytes);
 
 /* Work split of fa_fwd_host. */
 #define FA_HOST_DEFAULT_CHUNKS 8

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_version_and_strerror(lib):
     assert lib.fa_version() == 100
-    for code in range(0, -12, -1):
+    for code in range(0, -15, -1):
         msg = fa.fa_strerror(code)
         assert msg and msg != "unknown error code"
     assert fa.fa_strerror(-999) == "unknown error code"
@@ -182,3 +182,39 @@ def test_fa_fwd_variant_argument_errors(lib):
         assert (2 + x["stages"]) * tile + 9 * 1024 <= 227 * 1024
     i = ctypes.c_int()
     assert lib.fa_variant_info(len(vs), *[ctypes.byref(i)] * 5) == fa.FA_ERR_OPTION
+
+
+def test_fa_bwd_argument_errors(lib):
+    """The backward checks its arguments and workspace before any device
+    call; the workspace size follows its documented formula."""
+    DO, DQ, DK, DV, WS = 0x60000000, 0x70000000, 0x80000000, 0x90000000, 0xA0000000
+    need = fa.fa_bwd_workspace_size(2, 3, 1000, 128)
+    assert need == 2 * 3 * 1024 * (4 * 128 + 8)
+    assert fa.fa_bwd_workspace_size(1, 1, 1, 64) == 128 * (4 * 64 + 8)
+
+    def bwd(ws_bytes=None, **kw):
+        a = dict(q=Q, k=K, v=V, o=O, lse=L, do=DO, dq=DQ, dk=DK, dv=DV, ws=WS, B=2, H=3,
+                 N=1000, d=128, causal=0, scale=0.125, fp16=0)
+        a.update(kw)
+        nb = need if ws_bytes is None else ws_bytes
+        return lib.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"],
+                          a["dv"], a["ws"], nb, a["B"], a["H"], a["N"], a["d"], a["causal"],
+                          a["scale"], a["fp16"], None)
+    assert bwd(do=None) == fa.FA_ERR_NULL
+    assert bwd(ws=None) == fa.FA_ERR_NULL
+    assert bwd(N=0) == fa.FA_ERR_SHAPE
+    assert bwd(d=96) == fa.FA_ERR_HEADDIM
+    assert bwd(N=fa.FA_MAX_N + 1) == fa.FA_ERR_UNSUPPORTED_N
+    assert bwd(B=256, H=256, N=128) == fa.FA_ERR_SHAPE  # more than 65535 heads
+    assert bwd(dq=DQ + 8) == fa.FA_ERR_ALIGN
+    assert bwd(ws=WS + 128) == fa.FA_ERR_ALIGN
+    assert bwd(scale=0.0) == fa.FA_ERR_SCALE
+    assert bwd(ws_bytes=need - 1) == fa.FA_ERR_WORKSPACE
+    assert bwd(dq=Q) == fa.FA_ERR_ALIAS
+    assert bwd(dv=DK) == fa.FA_ERR_ALIAS
+    assert bwd(ws=DO) == fa.FA_ERR_ALIAS
+    assert bwd(dk=WS + 4096) == fa.FA_ERR_ALIAS
+    assert bwd(lse=DV + 64) == fa.FA_ERR_ALIAS
+    n = ctypes.c_size_t()
+    assert lib.fa_bwd_workspace_size(1, 1, 128, 64, None) == fa.FA_ERR_NULL
+    assert lib.fa_bwd_workspace_size(1, 1, 128, 32, ctypes.byref(n)) == fa.FA_ERR_HEADDIM

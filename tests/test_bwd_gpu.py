@@ -1,0 +1,154 @@
+"""GPU parity of the backward (fa_bwd, through the C ABI) against the fp64
+CPU oracle on identical seeded inputs.
+
+The GPU backward takes the GPU forward's O and LSE (as a caller would) and
+an output gradient dO ~ N(0,1); the oracle differentiates the definition
+from Q, K, V and dO alone.  The target states tolerances for the forward
+only; the bar here follows from the arithmetic: the kernel rounds P and dS
+to the 16-bit input type for its tensor-core products and the outputs to
+16 bits, each a relative error of at most 2^-9 (bf16) whose contributions
+average out over the sums, and D = rowsum(dO * O) uses the rounded O.  So
+per gradient tensor G: ||dG||_F <= 1e-2 ||G||_F (five times one bf16
+rounding) and max |dG| <= 2e-2 max |G|.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attn_inputs import make_qkv
+
+pytestmark = pytest.mark.gpu
+
+REL_FRO, REL_MAX = 1e-2, 2e-2
+
+
+def fa():
+    import exact_attention_forward_07_gb300 as m
+    return m
+
+
+def grad_inputs(B, H, N, d, dtype, seed, k_mult=1.0):
+    q, k, v = make_qkv(B, H, N, d, dtype, seed=seed, k_mult=k_mult)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 3)
+    do = torch.randn((B, H, N, d), generator=g, dtype=torch.float32).to(dtype)
+    return q, k, v, do
+
+
+def run_gpu_bwd(q, k, v, do, causal, scale=None):
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    o, lse = fa().forward(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = fa().backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa().fa_get_status() == 0
+    return [x.float().cpu().numpy() for x in (dq, dk, dv)]
+
+
+def assert_grads_close(got, ref, what):
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        assert np.all(np.isfinite(g)), f"{what} {name}: non-finite"
+        err = g - r
+        fro = np.linalg.norm(err) / max(np.linalg.norm(r), 1e-30)
+        mx = np.abs(err).max() / max(np.abs(r).max(), 1e-30)
+        assert fro <= REL_FRO and mx <= REL_MAX, f"{what} {name}: rel Fro {fro:.3g}, rel max {mx:.3g}"
+
+
+SMALL = [
+    (1, 1, 128, 64, torch.bfloat16),
+    (1, 1, 1, 64, torch.bfloat16),
+    (1, 2, 200, 128, torch.bfloat16),
+    (2, 2, 333, 64, torch.float16),
+    (1, 3, 384, 128, torch.bfloat16),
+    (2, 1, 1000, 128, torch.float16),
+    (1, 2, 2048 + 77, 128, torch.bfloat16),
+    (2, 2, 1024, 64, torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("B,H,N,d,dtype", SMALL,
+                         ids=[f"b{b}h{h}n{n}d{d}-{str(t)[6:]}" for b, h, n, d, t in SMALL])
+def test_bwd_parity_full_tensor(B, H, N, d, dtype, causal):
+    q, k, v, do = grad_inputs(B, H, N, d, dtype, seed=800 + N + d)
+    got = run_gpu_bwd(q, k, v, do, causal)
+    ref = oracle.attn_bwd(q, k, v, do, causal, 1.0 / math.sqrt(d))
+    assert_grads_close(got, ref, f"{B},{H},{N},{d},{dtype},causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_bwd_parity_bench_shape_heads(causal):
+    """[8,16,4096,128] bf16, the forward's gate shape: the whole launch on
+    the GPU, three spread heads (every row of them) against the oracle."""
+    B, H, N, d = 8, 16, 4096, 128
+    q, k, v, do = grad_inputs(B, H, N, d, torch.bfloat16, seed=900)
+    got = run_gpu_bwd(q, k, v, do, causal)
+    heads = [0, 61, 127]
+    sub = [x.reshape(B * H, 1, N, d)[heads].reshape(1, len(heads), N, d) for x in (q, k, v, do)]
+    ref = oracle.attn_bwd(*sub, causal, 1.0 / math.sqrt(d))
+    got = [g.reshape(B * H, N, d)[heads].reshape(1, len(heads), N, d) for g in got]
+    assert_grads_close(got, ref, f"[8,16,4096,128] causal={causal}")
+
+
+def test_bwd_peaked_rows_fp16():
+    """K scaled x4 (the peaked fp16 workload's values): P close to one-hot."""
+    q, k, v, do = grad_inputs(1, 2, 1024, 128, torch.float16, seed=901, k_mult=4.0)
+    for causal in (False, True):
+        got = run_gpu_bwd(q, k, v, do, causal)
+        ref = oracle.attn_bwd(q, k, v, do, causal, 1.0 / math.sqrt(128))
+        assert_grads_close(got, ref, f"peaked causal={causal}")
+
+
+def test_bwd_closed_forms():
+    """One key: dV = dO and dQ = dK = 0.  Constant V rows: dQ = dK = 0."""
+    q, k, v, do = grad_inputs(2, 3, 1, 64, torch.bfloat16, seed=902)
+    dq, dk, dv = run_gpu_bwd(q, k, v, do, False)
+    assert np.max(np.abs(dv - do.float().numpy())) <= 1e-2
+    # dS = P (dO.v - D): D is the same dot product summed in another order
+    assert np.max(np.abs(dq)) <= 1e-3 and np.max(np.abs(dk)) <= 1e-3
+    q, k, _, do = grad_inputs(1, 2, 300, 128, torch.bfloat16, seed=903)
+    v = torch.linspace(-2, 2, 128).to(torch.bfloat16).expand(1, 2, 300, 128).contiguous()
+    for causal in (False, True):
+        dq, dk, _ = run_gpu_bwd(q, k, v, do, causal)
+        # dS = P (dO.v - dO.o) with o = v up to O's rounding: tiny, not exact
+        assert np.max(np.abs(dq)) <= 2e-2 and np.max(np.abs(dk)) <= 2e-2
+
+
+def test_bwd_dk_dv_bitwise_repeatable():
+    """dK and dV come from a fixed order of MMAs: bitwise the same on a
+    second run.  dQ is added up with atomics in any order: close."""
+    q, k, v, do = grad_inputs(2, 4, 1536, 128, torch.bfloat16, seed=904)
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    for causal in (False, True):
+        o, lse = fa().forward(qd, kd, vd, causal=causal)
+        a = fa().backward(qd, kd, vd, o, lse, dod, causal=causal)
+        b = fa().backward(qd, kd, vd, o, lse, dod, causal=causal)
+        torch.cuda.synchronize()
+        assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+        assert torch.allclose(a[0].float(), b[0].float(), rtol=1e-2, atol=1e-3)
+    assert fa().fa_get_status() == 0
+
+
+def test_bwd_reused_workspace_and_side_stream():
+    """A workspace left dirty by one call serves the next (nothing needs to
+    be cleared); calls on a side stream."""
+    q, k, v, do = grad_inputs(1, 2, 700, 64, torch.bfloat16, seed=905)
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    ws = torch.full((fa().fa_bwd_workspace_size(1, 2, 700, 64),), 0x7F, dtype=torch.uint8,
+                    device=dev)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    ref = oracle.attn_bwd(q, k, v, do, True, 0.3)
+    with torch.cuda.stream(s):
+        o, lse = fa().forward(qd, kd, vd, causal=True, scale=0.3, stream=s)
+        for _ in range(2):
+            dq, dk, dv = (torch.empty_like(qd) for _ in range(3))
+            fa().fa_bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, ws, causal=True, scale=0.3, stream=s)
+            s.synchronize()
+            assert_grads_close([x.float().cpu().numpy() for x in (dq, dk, dv)], ref, "reuse")
+    assert fa().fa_get_status() == 0
