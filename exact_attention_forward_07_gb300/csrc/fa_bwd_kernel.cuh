@@ -23,19 +23,19 @@
 //                        TMA ring of Q_i and dO_i; five tcgen05 MMAs per step
 //   fa_bwd_dq_kernel     dQ = scale * accumulators, rounded to 16 bits
 //
-// Roles in fa_bwd_kernel (512 threads):
+// Roles in fa_bwd_kernel (640 threads):
 //   warp  0     TMA producer (one thread)
 //   warp  1     MMA issue (one elected lane) + tensor-memory allocation
-//   warps 4-11  dS warps: warp w owns the keys of lane quadrant w % 4 (one
-//               thread per key) and half of the query columns; they form
-//               P^T and dS^T, then write the block's dK and dV
-//   warps 12-15 dQ warps: read each step's dQ out of tensor memory (one
-//               thread per query row) and add it to the fp32 accumulators
+//   warps 4-19  compute warps: warp w owns lane quadrant w % 4 and a slice
+//               of 32 columns; per step they form P^T and dS^T (one thread
+//               per key), then read dQ out of tensor memory (one thread per
+//               query row) and add it to the fp32 accumulators; at the end
+//               they write the block's dK and dV
 //
 // Per step (query block i):
 //   S^T  = K_j Q_i^T      SS  -> TMEM [0,128)     (lanes = keys)
 //   dP^T = V_j dO_i^T     SS  -> TMEM [128,256)
-//   dS warps: P^T = 2^(S^T scale log2e - lse2_i), packed to 16 bits over
+//   compute warps: P^T = 2^(S^T scale log2e - lse2_i), packed to 16 bits over
 //   S^T; dS^T = P^T (dP^T - D_i) to shared memory, 128-byte swizzled
 //   dV  += P^T dO_i       TS  (P^T from TMEM, dO_i MN-major)
 //   dK  += dS^T Q_i       SS  (dS^T K-major, Q_i MN-major)
@@ -44,8 +44,8 @@
 // K-major layout of dS^T (rows = keys) and the MN-major layout of dS (64
 // queries per swizzled row, keys along the rows), so one store serves both
 // MMAs.  dQ goes to the columns of dP^T at d = 128 (tensor memory is full:
-// S, dP, dK and dV take 512 columns), so the next dP^T waits until the dQ
-// warps have read it; at d = 64 it has columns of its own.
+// S, dP, dK and dV take 512 columns), so the next dP^T waits until the
+// compute warps have read it; at d = 64 it has columns of its own.
 //
 // Every wait is bounded as in the forward kernel; a wait that gives up sets
 // the abort flag and the status word, in-flight copies and MMAs are drained
@@ -87,8 +87,8 @@ struct BwdCfg {
   static constexpr int kDd = kLse + 2 * 512;    // [stage][128] fp32
   static constexpr int kBar = kDd + 2 * 512;
   // barriers: K/V loaded; Q/dO stage full (2) and empty (2); S^T and dP^T
-  // done; dS written (8 arrivals); dQ done; dQ read (4 arrivals); dK/dV done;
-  // drain
+  // done; dS written and dQ read (one arrival per compute warp each); dQ
+  // done; dK/dV done; drain
   static constexpr int bKV = 0, bFull = 1, bEmpty = 3, bSdp = 5, bDs = 6, bDqFull = 7,
                        bDqFree = 8, bDkdv = 9, bDrain = 10, kNumBars = 11;
   static constexpr int kMisc = kBar + kNumBars * 8;  // tmem base, abort flag
@@ -107,7 +107,8 @@ struct BwdCfg {
   static constexpr uint32_t kIdescS = idesc_f16(BF16, false, 128, 128);         // S^T, dP^T
   static constexpr uint32_t kIdescG = idesc_f16(BF16, true, 128, D);            // dV, dK
   static constexpr uint32_t kIdescQ = idesc_f16_ab(BF16, true, true, 128, D);   // dQ
-  static constexpr int kThreads = 512;
+  static constexpr int kThreads = 640;
+  static constexpr int kComputeWarps = 16;
 };
 
 // D and lse * log2(e) for one 128-row tile of one head, and that tile's
@@ -225,9 +226,9 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       mbar_init(bar(C::bEmpty + s), 1);
     }
     mbar_init(bar(C::bSdp), 1);
-    mbar_init(bar(C::bDs), 8);      // one arrival per dS warp
+    mbar_init(bar(C::bDs), C::kComputeWarps);      // one arrival per compute warp
     mbar_init(bar(C::bDqFull), 1);
-    mbar_init(bar(C::bDqFree), 4);  // one arrival per dQ warp
+    mbar_init(bar(C::bDqFree), C::kComputeWarps);  // one arrival per compute warp
     mbar_init(bar(C::bDkdv), 1);
     mbar_init(bar(C::bDrain), 1);
     *abort_flag = 0;
@@ -312,11 +313,11 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       mma_commit_if(leader, bar(C::bSdp));
       if (!(ok = wait_bar(bar(C::bDs), t & 1u, abort_flag, p.status))) break;
       tc_fence_after();
-      // dV += P^T dO: P^T packed in tensor memory, half h of the queries at
-      // columns [64h, 64h + 32)
+      // dV += P^T dO: P^T packed in tensor memory, query slice c (32
+      // queries) at columns [32c, 32c + 16)
       const uint64_t bdo = mdesc0 + (do_s >> 4), bq = mdesc0 + (q_s >> 4);
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts_if(leader, tmem + C::cDV, tmem + C::cS + 64 * (kk >> 2) + 8 * (kk & 3),
+        mma_ts_if(leader, tmem + C::cDV, tmem + C::cS + 32 * (kk >> 1) + 8 * (kk & 1),
                   bdo + kk * (2048 >> 4), C::kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
       // dK += dS^T Q: dS^T K-major in shared memory, Q MN-major
       const uint64_t ads = kdesc0 + ((sbase + C::kDS) >> 4);
@@ -340,15 +341,22 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     if (ok) mma_commit_if(leader, bar(C::bDkdv));
     mma_commit_if(leader, bar(C::bDrain));
     wait_drain(bar(C::bDrain), 0, abort_flag, p.status);
-  } else if (warp >= 4 && warp < 12) {
-    // -------------------------------------------------------------- dS warps
+  } else if (warp >= 4) {
+    // --------------------------------------------------------- compute warps
+    // Sixteen warps; warp w owns the keys of lane quadrant w % 4 (one thread
+    // per key) and the 32 query columns [32 cs, 32 cs + 32) of S^T, dP^T,
+    // P^T and dS^T, cs = (w - 4) / 4; then the same 32 columns of dQ for
+    // the query rows of its quadrant.  The two phases of a step never
+    // overlap (the next dP^T waits for dQ at d = 128), so one pool of warps
+    // runs both, each on a quarter of the columns.
     const int w = warp - 4;
-    const int qd = w & 3, hf = w >> 2;  // lane quadrant (keys), half of the query columns
-    const int row = qd * 32 + static_cast<int>(lane);  // key within the block
+    const int qd = w & 3, cs = w >> 2;
+    const int row = qd * 32 + static_cast<int>(lane);  // key (phase 1) / query (phase 2)
     const bool key_dead = jb * 128 + row >= p.N;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(qd * 32) << 16);
     const uint64_t sl2_2 = f2(p.scale_log2, p.scale_log2);
-    uint8_t *ds_row = smem + C::kDS + hf * C::kHalf + row * 128;
+    // this key's 128-byte row of dS^T in half cs / 2 of the query columns
+    uint8_t *ds_row = smem + C::kDS + (cs >> 1) * C::kHalf + row * 128;
     bool ok = true;
     for (int t = 0; ok && t < n_steps; ++t) {
       if (!(ok = wait_bar(bar(C::bSdp), t & 1u, abort_flag, p.status))) break;
@@ -358,16 +366,16 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       const float *dds = reinterpret_cast<const float *>(smem + C::kDd + s * 512);
       const bool diag = p.causal && i == jb;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int q0 = 64 * hf + 32 * c;  // first query column of this chunk
-        uint32_t sr[32], dr[32];
-        tmem_ld32(t_lane + C::cS + q0, sr);
-        tmem_ld32(t_lane + C::cDP + q0, dr);
+      for (int sc = 0; sc < 2; ++sc) {
+        const int q0 = 32 * cs + 16 * sc;  // first query column of this sub-chunk
+        uint32_t sr[16], dr[16];
+        tmem_ld16(t_lane + C::cS + q0, sr);
+        tmem_ld16(t_lane + C::cDP + q0, dr);
         tmem_ld_wait(sr);
         tmem_ld_wait(dr);
-        uint32_t pk[16], dk[16];
+        uint32_t pk[8], gk[8];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
+        for (int e = 0; e < 16; e += 4) {
           const float4 l4 = *reinterpret_cast<const float4 *>(lse2s + q0 + e);
           const float4 d4 = *reinterpret_cast<const float4 *>(dds + q0 + e);
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
@@ -385,18 +393,19 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
                                              f2(-dv[u], -dv[u + 1]))),
                      g0, g1);
             pk[(e + u) >> 1] = pack2<BF16>(p0, p1);
-            dk[(e + u) >> 1] = pack2<BF16>(g0, g1);
+            gk[(e + u) >> 1] = pack2<BF16>(g0, g1);
           }
         }
-        // P^T of these 32 queries: 16 packed columns over this chunk's own S^T
-        tmem_st16(t_lane + C::cS + 64 * hf + 16 * c, pk);
-        // dS^T: 64 bytes of the key's 128-byte row in this half, chunks
-        // 4c..4c+3 at their 128-byte-swizzle positions
+        // P^T of these 16 queries: 8 packed columns over this slice's own
+        // S^T (columns 32 cs + 8 sc), already loaded
+        tmem_st8(t_lane + C::cS + 32 * cs + 8 * sc, pk);
+        // dS^T: 32 bytes of the key's row, 16-byte chunks at their
+        // 128-byte-swizzle positions
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int pos = (4 * c + u) ^ (row & 7);
+        for (int u = 0; u < 2; ++u) {
+          const int pos = (4 * (cs & 1) + 2 * sc + u) ^ (row & 7);
           *reinterpret_cast<uint4 *>(ds_row + 16 * pos) =
-              make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+              make_uint4(gk[4 * u], gk[4 * u + 1], gk[4 * u + 2], gk[4 * u + 3]);
         }
       }
       tmem_st_wait();
@@ -404,60 +413,62 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::bDs));
+      // phase 2: dQ of this step (query rows of this quadrant, 32 columns)
+      // into registers; its tensor-memory columns are released before the
+      // additions are issued, so the next step's MMAs overlap them
+      if (!(ok = wait_bar(bar(C::bDqFull), t & 1u, abort_flag, p.status))) break;
+      tc_fence_after();
+      uint32_t r[32];
+      if (32 * cs < D) {
+        tmem_ld32(t_lane + C::cDQ + 32 * cs, r);
+        tmem_ld_wait(r);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::bDqFree));
+      if (32 * cs < D) {
+        float4 *dst = p.dq_acc + (static_cast<size_t>(bh) * T + i) * (D / 4) * 128 + row +
+                      8 * cs * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          red_add_v4(dst + u * 128, __uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                     __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+      }
     }
-    // epilogue: dK (times scale) and dV of this warp's keys, half the columns
+    // epilogue: dK (times scale) and dV of this quadrant's keys; 32 columns
+    // each: d = 128, slice cs of both; d = 64, slices 0-1 take dK and 2-3 dV
     ok = __all_sync(0xffffffffu, ok);
     if (ok) ok = wait_bar(bar(C::bDkdv), 0, abort_flag, p.status);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after();
       const int key0 = jb * 128 + qd * 32;  // key of lane 0
-      const size_t off = (static_cast<size_t>(bh) * p.N + key0) * D + (D / 2) * hf;
+#pragma unroll
       for (int g = 0; g < 2; ++g) {
-        uint8_t *row0 = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(g ? p.dv : p.dk) + off);
-        const float mul = g ? 1.f : p.scale;
-        const uint32_t col = (g ? C::cDV : C::cDK) + (D / 2) * hf;
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t r[32];
-          tmem_ld32(t_lane + col + 32 * c, r);
-          tmem_ld_wait(r);
-          uint4 v4[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            v4[u] = make_uint4(pack2<BF16>(__uint_as_float(r[8 * u]) * mul, __uint_as_float(r[8 * u + 1]) * mul),
-                               pack2<BF16>(__uint_as_float(r[8 * u + 2]) * mul, __uint_as_float(r[8 * u + 3]) * mul),
-                               pack2<BF16>(__uint_as_float(r[8 * u + 4]) * mul, __uint_as_float(r[8 * u + 5]) * mul),
-                               pack2<BF16>(__uint_as_float(r[8 * u + 6]) * mul, __uint_as_float(r[8 * u + 7]) * mul));
-          store_rows<4>(v4, row0 + 64 * c, static_cast<size_t>(D) * 2, p.N - key0, lane);
+        int colx;  // first of the 32 columns this warp writes, or -1
+        if constexpr (D == 128) {
+          colx = 32 * cs;
+        } else {
+          colx = ((cs >> 1) == g) ? 32 * (cs & 1) : -1;
         }
+        if (colx < 0) continue;
+        uint8_t *row0 = reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(g ? p.dv : p.dk) +
+                                                    (static_cast<size_t>(bh) * p.N + key0) * D + colx);
+        const float mul = g ? 1.f : p.scale;
+        uint32_t r[32];
+        tmem_ld32(t_lane + (g ? C::cDV : C::cDK) + colx, r);
+        tmem_ld_wait(r);
+        uint4 v4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          v4[u] = make_uint4(pack2<BF16>(__uint_as_float(r[8 * u]) * mul, __uint_as_float(r[8 * u + 1]) * mul),
+                             pack2<BF16>(__uint_as_float(r[8 * u + 2]) * mul, __uint_as_float(r[8 * u + 3]) * mul),
+                             pack2<BF16>(__uint_as_float(r[8 * u + 4]) * mul, __uint_as_float(r[8 * u + 5]) * mul),
+                             pack2<BF16>(__uint_as_float(r[8 * u + 6]) * mul, __uint_as_float(r[8 * u + 7]) * mul));
+        store_rows<4>(v4, row0, static_cast<size_t>(D) * 2, p.N - key0, lane);
       }
     }
     tc_fence_before();
-  } else if (warp >= 12) {
-    // -------------------------------------------------------------- dQ warps
-    const int qd = warp & 3;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(qd * 32) << 16);
-    bool ok = true;
-    for (int t = 0; ok && t < n_steps; ++t) {
-      if (!(ok = wait_bar(bar(C::bDqFull), t & 1u, abort_flag, p.status))) break;
-      tc_fence_after();
-      const int i = i0 + t;
-      float4 *dst = p.dq_acc + (static_cast<size_t>(bh) * T + i) * (D / 4) * 128 + qd * 32 + lane;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(t_lane + C::cDQ + 32 * c, r);
-        tmem_ld_wait(r);
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          red_add_v4(dst + (8 * c + u) * 128, __uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
-                     __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::bDqFree));
-    }
   }
 
   __syncthreads();

@@ -9,7 +9,10 @@ to the 16-bit input type for its tensor-core products and the outputs to
 16 bits, each a relative error of at most 2^-9 (bf16) whose contributions
 average out over the sums, and D = rowsum(dO * O) uses the rounded O.  So
 per gradient tensor G: ||dG||_F <= 1e-2 ||G||_F (five times one bf16
-rounding) and max |dG| <= 2e-2 max |G|.
+rounding) and max |dG| <= 2e-2 max |G|, with ||G||_F and max |G| floored at
+1e-3 sqrt(size) and 1e-3 (the gradients of these N(0,1) inputs are of order
+0.1 to 1; the floor only matters where the exact gradient is zero, e.g. dQ
+and dK with a single key).
 """
 import math
 
@@ -52,8 +55,8 @@ def assert_grads_close(got, ref, what):
     for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
         assert np.all(np.isfinite(g)), f"{what} {name}: non-finite"
         err = g - r
-        fro = np.linalg.norm(err) / max(np.linalg.norm(r), 1e-30)
-        mx = np.abs(err).max() / max(np.abs(r).max(), 1e-30)
+        fro = np.linalg.norm(err) / max(np.linalg.norm(r), 1e-3 * math.sqrt(r.size))
+        mx = np.abs(err).max() / max(np.abs(r).max(), 1e-3)
         assert fro <= REL_FRO and mx <= REL_MAX, f"{what} {name}: rel Fro {fro:.3g}, rel max {mx:.3g}"
 
 
