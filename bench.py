@@ -38,7 +38,9 @@ and dtype, R rounds in alternating order, and prints a Markdown table of
 median TFLOPS, median SM clock and FLOP per SM clock (the clock-normalised
 rate, which removes the power limit's effect on the clock).
 `--rescale-stats` runs the counting build once and prints how often the
-online softmax's O rescale fired.
+online softmax's O rescale fired.  `host_us_per_call` in the line is the
+host time to enqueue one call (argument checks, tensor maps, launch),
+measured around the timed launch loop before its final synchronisation.
 
 `--pass bwd` times the backward pass instead (fa_bwd: dQ, dK, dV from the
 forward's O and LSE and a seeded output gradient, three kernels per step;
@@ -71,7 +73,7 @@ METRIC = "attention fwd TFLOPS (bf16, 1×GB300) and fraction of dense tensor-cor
 METRIC_BWD = "attention bwd TFLOPS (bf16, 1×GB300) and fraction of dense tensor-core peak"
 DEFAULT_WORKLOAD = "b1h32n16384d128_causal"
 FALLBACK_BF16_TFLOPS = 1900.0
-KERNEL_SOURCES = ["fa_api.cu", "fa_kernel.cuh", "ptx.cuh"]
+KERNEL_SOURCES = ["fa_api.cu", "fa_kernel.cuh", "fa_bwd_kernel.cuh", "ptx.cuh"]
 AUTO_TIMED_S = 2.0  # timed work with no --steps
 SUSTAINED_AFTER_S = 1.0  # timed regions at least this long compare against the sustained peak
 CPU_SAMPLE_FLOP = 1.1e12  # oracle work of the default cpu_baseline sample (~17 s on 16 cores)
@@ -466,8 +468,10 @@ def run_ours(args, w):
     ev1 = torch.cuda.Event(enable_timing=True)
     t_begin = time.time()
     ev0.record(stream)
+    h0 = time.perf_counter()
     for _ in range(args.steps):
         call(q, k, v, o, lse, causal=w.causal, stream=stream)
+    host_us = (time.perf_counter() - h0) / args.steps * 1e6  # enqueue time per call
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     t_end = time.time()
@@ -565,6 +569,7 @@ def run_ours(args, w):
                        l2=l2_note(w), **({"variant": variant} if variant else {}),
                        **({"pass": "bwd"} if bwd else {})),
         "gpu_launches": args.steps * (3 if bwd else 1),
+        "host_us_per_call": host_us,
         "clocks": clocks,
         "roofline": roofline,
         "cpu_baseline": cpu,

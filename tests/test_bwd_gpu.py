@@ -22,6 +22,7 @@ import torch
 
 import oracle
 from attn_inputs import make_qkv
+from tests.margins import record
 
 pytestmark = pytest.mark.gpu
 
@@ -57,6 +58,7 @@ def assert_grads_close(got, ref, what):
         err = g - r
         fro = np.linalg.norm(err) / max(np.linalg.norm(r), 1e-3 * math.sqrt(r.size))
         mx = np.abs(err).max() / max(np.abs(r).max(), 1e-3)
+        record("bwd", f"{what} {name}", rel_fro=fro, rel_max=mx)
         assert fro <= REL_FRO and mx <= REL_MAX, f"{what} {name}: rel Fro {fro:.3g}, rel max {mx:.3g}"
 
 

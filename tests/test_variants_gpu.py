@@ -12,6 +12,7 @@ import torch
 
 import oracle
 from attn_inputs import make_qkv
+from tests.margins import record
 
 pytestmark = pytest.mark.gpu
 
@@ -39,6 +40,7 @@ def _check(o, lse, o_ref, lse_ref, what):
     d_o = np.abs(o - o_ref)
     d_l = np.abs(lse - lse_ref) / np.maximum(1.0, np.abs(lse_ref))
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), what
+    record("variant", what, max_abs_o=d_o.max(), mean_abs_o=d_o.mean(), max_rel_lse=d_l.max())
     assert d_o.max() <= O_MAX and d_o.mean() <= O_MEAN and d_l.max() <= LSE_REL, (
         f"{what}: max|dO| {d_o.max():.3g} mean|dO| {d_o.mean():.3g} rel dLSE {d_l.max():.3g}")
 
