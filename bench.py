@@ -553,7 +553,7 @@ def run_ours(args, w):
         if n_heads <= 0:  # about CPU_SAMPLE_FLOP of oracle work: whole heads
             n_heads = max(1, round(CPU_SAMPLE_FLOP / (flops / (w.B * w.H))))
         if bwd:
-            tf, dt, desc = oracle_bwd_sample(w, *q64, do_h, n_heads=max(1, n_heads // 2))
+            tf, dt, desc = oracle_bwd_sample(w, *q64, do_h, n_heads=n_heads)
         else:
             tf, dt, desc = oracle_sample(w, *q64, n_heads=n_heads)
         cpu = {"value": tf, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
