@@ -79,9 +79,9 @@ SUSTAINED_AFTER_S = 1.0  # timed regions at least this long compare against the 
 CPU_SAMPLE_FLOP = 1.1e12  # oracle work of the default cpu_baseline sample (~17 s on 16 cores)
 
 
-def profile_summary(workload: str) -> str:
-    """The committed ncu summary of the kernel on a workload."""
-    return os.path.join(ROOT, "profiles", f"fa_fwd_kernel_{workload}.md")
+def profile_summary(workload: str, kernel: str = "fa_fwd_kernel") -> str:
+    """The committed ncu summary of a kernel on a workload."""
+    return os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
 
 
 def dist_env():
@@ -109,12 +109,12 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary of `workload`,
-    or None when there is none or the kernel sources changed since that
-    capture."""
+def profiled_traffic(workload: str, kernel: str = "fa_fwd_kernel"):
+    """DRAM bytes per launch from the committed ncu summary of `kernel` on
+    `workload`, or None when there is none or the kernel sources changed
+    since that capture."""
     try:
-        text = open(profile_summary(workload)).read()
+        text = open(profile_summary(workload, kernel)).read()
     except OSError:
         return None
     m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
@@ -543,8 +543,8 @@ def run_ours(args, w):
                 "traffic": profiled_traffic(w.name),
                 "kernel": "%s<%d,%s>" % ("fa_bwd_kernel" if bwd else "fa_fwd_kernel", w.d,
                                          "bf16" if w.dtype == "bf16" else "fp16")}
-    if bwd:  # no committed ncu summary of the backward is tied to this number
-        roofline["traffic"] = profiled_traffic("bwd_" + w.name)
+    if bwd:  # the main backward kernel's summary (the row kernels are a few percent)
+        roofline["traffic"] = profiled_traffic(w.name, "fa_bwd_kernel")
 
     cpu = None
     if not args.no_cpu_baseline:
