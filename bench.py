@@ -39,8 +39,10 @@ median TFLOPS, median SM clock and FLOP per SM clock (the clock-normalised
 rate, which removes the power limit's effect on the clock).
 `--rescale-stats` runs the counting build once and prints how often the
 online softmax's O rescale fired.  `host_us_per_call` in the line is the
-host time to enqueue one call (argument checks, tensor maps, launch),
-measured around the timed launch loop before its final synchronisation.
+host time to enqueue one call through the Python binding, measured around
+the timed launch loop before its final synchronisation;
+`host_us_per_call_c_abi` the same for 50 direct C-ABI calls (argument
+checks, cached tensor maps, launch).
 
 `--pass bwd` times the backward pass instead (fa_bwd: dQ, dK, dV from the
 forward's O and LSE and a seeded output gradient, three kernels per step;
@@ -485,6 +487,21 @@ def run_ours(args, w):
     status = fa.fa_get_status(stream)
     if status != 0:
         raise RuntimeError(f"kernel status {status}: {fa.fa_strerror(status)}")
+    # The library's own enqueue cost: the C ABI called through ctypes with
+    # its arguments built beforehand (forward, default variant), 50 calls.
+    c_abi_us = None
+    if not bwd and not variant:
+        import ctypes
+        fn = fa.lib().fa_fwd if w.dtype == "bf16" else fa.lib().fa_fwd_fp16
+        cargs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                 w.B, w.H, w.N, w.d, int(w.causal), ctypes.c_float(w.scale),
+                 ctypes.c_void_p(stream.cuda_stream))
+        torch.cuda.synchronize(dev)
+        h0 = time.perf_counter()
+        for _ in range(50):
+            fn(*cargs)
+        c_abi_us = (time.perf_counter() - h0) / 50 * 1e6
+        torch.cuda.synchronize(dev)
 
     # ------------------------------------------------ end to end, host buffers
     # Pinned host Q, K, V in; pinned host O, LSE out; every step is one
@@ -570,6 +587,7 @@ def run_ours(args, w):
                        **({"pass": "bwd"} if bwd else {})),
         "gpu_launches": args.steps * (3 if bwd else 1),
         "host_us_per_call": host_us,
+        "host_us_per_call_c_abi": c_abi_us,
         "clocks": clocks,
         "roofline": roofline,
         "cpu_baseline": cpu,

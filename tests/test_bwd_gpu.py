@@ -157,3 +157,28 @@ def test_bwd_reused_workspace_and_side_stream():
             s.synchronize()
             assert_grads_close([x.float().cpu().numpy() for x in (dq, dk, dv)], ref, "reuse")
     assert fa().fa_get_status() == 0
+
+
+def test_bwd_cuda_graph_capture_replays():
+    """fa_bwd allocates nothing and runs on the caller's stream, so it can be
+    captured into a CUDA graph: replays give the eager dK and dV bit for bit
+    and dQ up to the order of its additions."""
+    q, k, v, do = grad_inputs(1, 3, 1000, 128, torch.bfloat16, seed=906)
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    o, lse = fa().forward(qd, kd, vd, causal=True)
+    ref = fa().backward(qd, kd, vd, o, lse, dod, causal=True)
+    dq, dk, dv = (torch.empty_like(qd) for _ in range(3))
+    ws = torch.empty(fa().fa_bwd_workspace_size(1, 3, 1000, 128), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fa().fa_bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, ws, causal=True)
+    for _ in range(2):
+        for x in (dq, dk, dv):
+            x.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
+        assert torch.allclose(dq.float(), ref[0].float(), rtol=1e-2, atol=1e-3)
+    assert fa().fa_get_status() == 0
