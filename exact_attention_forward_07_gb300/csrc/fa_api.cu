@@ -70,8 +70,10 @@ struct DeviceState {
   cudaEvent_t host_ev[3][3] = {};  // [slot][loaded, done, drained]
   uint8_t *stage = nullptr;
   size_t stage_bytes = 0;
-  std::once_flag attr_once[kMaxVariants];  // shared-memory attribute, per kernel variant
-  int attr_err[kMaxVariants] = {};
+  // shared-memory attribute, per kernel instance: [variant] static rounds,
+  // [kMaxVariants + variant] per-CTA lists
+  std::once_flag attr_once[2 * kMaxVariants];
+  int attr_err[2 * kMaxVariants] = {};
   std::once_flag bwd_attr_once[4];  // backward kernels: [d == 128][fp16]
   int bwd_attr_err[4] = {};
 };
@@ -425,6 +427,7 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
            unsigned long long *stats, int order, const fa::SchedList *list, cudaStream_t stream) {
   using C = fa::Cfg<D, BF16, STAGES, EXPSPLIT, STATS>;
   auto kernel = fa::fa_fwd_kernel<D, BF16, STAGES, EXPSPLIT, STATS, LIST>;
+  if (LIST) slot += kMaxVariants;  // the list instance has attributes of its own
   std::call_once(ds.attr_once[slot], [&] {
     cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
