@@ -45,7 +45,6 @@ FA_HOST_MAX_CHUNKS = 1024
 FA_DEFAULT_RESCALE_THRESHOLD = 8.0
 FA_MAX_RESCALE_THRESHOLD = 12.0
 FA_ORDER_AUTO = -2
-FA_SCHEDULE_AUTO, FA_SCHEDULE_ROUNDS, FA_SCHEDULE_LISTS = 0, 1, 2
 
 _lib = None
 
@@ -84,7 +83,7 @@ def lib():
         L.fa_fwd_noalloc.restype = ctypes.c_int
         L.fa_fwd_variant.argtypes = [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int,
                                      ctypes.c_float, ctypes.c_int, ctypes.c_float, ctypes.c_int,
-                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P]
+                                     ctypes.c_int, ctypes.c_int, P, P]
         L.fa_fwd_variant.restype = ctypes.c_int
         L.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, I64, I64, I64, I64,
                              ctypes.c_int, ctypes.c_float, ctypes.c_int, P]
@@ -201,14 +200,13 @@ def fa_fwd_noalloc(q, k, v, o, lse, causal=False, scale=None, rescale_threshold=
 
 
 def fa_fwd_variant(q, k, v, o, lse, causal=False, scale=None, rescale_threshold=None,
-                   stages=0, exp_split=0, causal_order=FA_ORDER_AUTO,
-                   schedule=FA_SCHEDULE_AUTO, stats=None, stream=None) -> None:
+                   stages=0, exp_split=0, causal_order=FA_ORDER_AUTO, stats=None,
+                   stream=None) -> None:
     """Forward through one of the library's kernel variants (tuning and
     measurement): `stages` K/V ring slots (0 = default), every
     `exp_split`-th pair of exponentials on the FMA pipes (0 = none), a
     forced causal item order (-1, or g >= 0 tail heads; default: the
-    library's choice), a forced causal schedule (FA_SCHEDULE_ROUNDS or
-    FA_SCHEDULE_LISTS), and optional rescale counters `stats` (a CUDA int64
+    library's choice), and optional rescale counters `stats` (a CUDA int64
     tensor of 4, added to).  dtype from q (bf16/fp16)."""
     import torch
     if rescale_threshold is None:
@@ -224,7 +222,7 @@ def fa_fwd_variant(q, k, v, o, lse, causal=False, scale=None, rescale_threshold=
     fp16 = int(q.dtype == torch.float16)
     _call("fa_fwd_variant", q, k, v, o, lse, causal, scale, stream, q.dtype,
           extra=(fp16, float(rescale_threshold), int(stages), int(exp_split),
-                 int(causal_order), int(schedule), sp))
+                 int(causal_order), sp))
 
 
 def fa_bwd_workspace_size(B, H, N, d) -> int:

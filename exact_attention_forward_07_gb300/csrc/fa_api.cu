@@ -7,9 +7,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
-#include <memory>
 #include <mutex>
-#include <queue>
 #include <unordered_map>
 #include <vector>
 
@@ -24,17 +22,8 @@ __device__ unsigned g_fa_status = 0;  // per-device status word (FA_ERR_TIMEOUT 
 __device__ __align__(256) unsigned char g_fa_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-
-// How a causal launch takes its items: the order (-1: heaviest pair first
-// across all heads; g >= 0: head by head with the last g heads together)
-// and, when it balances better than the static rounds, per-CTA lists.
-struct CausalPlan {
-  int order = -1;
-  std::shared_ptr<fa::SchedList> list;
-};
 constexpr int kMaxVariants = 32;
 constexpr int kOrderAuto = -2;  // causal item order: the library's choice
-constexpr int kScheduleAuto = 0, kScheduleRounds = 1, kScheduleLists = 2;  // fa_fwd_variant
 
 struct DeviceState {
   std::once_flag once;
@@ -48,7 +37,7 @@ struct DeviceState {
   // causal item order chosen per (B*H, Q tiles): the host simulation runs
   // once per shape
   std::mutex order_mu;
-  std::unordered_map<uint64_t, CausalPlan> order_cache;  // per (B*H, Q tiles)
+  std::unordered_map<uint64_t, int> order_cache;  // causal_order's result
   // encoded TMA tensor maps, direct-mapped by (address, shape, dtype): a map
   // depends on nothing else, so a hit needs no re-encoding
   struct MapEntry {
@@ -70,10 +59,8 @@ struct DeviceState {
   cudaEvent_t host_ev[3][3] = {};  // [slot][loaded, done, drained]
   uint8_t *stage = nullptr;
   size_t stage_bytes = 0;
-  // shared-memory attribute, per kernel instance: [variant] static rounds,
-  // [kMaxVariants + variant] per-CTA lists
-  std::once_flag attr_once[2 * kMaxVariants];
-  int attr_err[2 * kMaxVariants] = {};
+  std::once_flag attr_once[kMaxVariants];  // shared-memory attribute, per kernel variant
+  int attr_err[kMaxVariants] = {};
   std::once_flag bwd_attr_once[4];  // backward kernels: [d == 128][fp16]
   int bwd_attr_err[4] = {};
 };
@@ -257,17 +244,6 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
-// Load of one causal item of each level (level 0 = the heaviest pair): the
-// larger tile's K/V blocks plus about 1.3 blocks of restart.
-std::vector<double> causal_item_loads(int n_qtiles, int n_pairs) {
-  std::vector<double> w(static_cast<size_t>(n_pairs));
-  for (int level = 0; level < n_pairs; ++level) {
-    const int qt1 = 2 * (n_pairs - 1 - level) + 1;
-    w[static_cast<size_t>(level)] = (qt1 < n_qtiles ? qt1 + 1 : qt1) + 1.3;
-  }
-  return w;
-}
-
 // Causal item order.  In round r of the static schedule CTA b takes item
 // r * G + b (even rounds) or r * G + G - 1 - b (odd rounds).  Taking the
 // heaviest pairs first across all heads balances the SMs best, but once the
@@ -287,7 +263,12 @@ std::vector<double> causal_item_loads(int n_qtiles, int n_pairs) {
 int causal_order(int BH, int n_qtiles, int n_pairs, int G, double kv_head_bytes) {
   const int64_t n = static_cast<int64_t>(BH) * n_pairs;
   if (n <= G || n > (int64_t(1) << 20)) return -1;
-  const std::vector<double> w = causal_item_loads(n_qtiles, n_pairs);
+  // load of one item of each level (level 0 = the heaviest pair)
+  std::vector<double> w(static_cast<size_t>(n_pairs));
+  for (int level = 0; level < n_pairs; ++level) {
+    const int qt1 = 2 * (n_pairs - 1 - level) + 1;
+    w[static_cast<size_t>(level)] = (qt1 < n_qtiles ? qt1 + 1 : qt1) + 1.3;
+  }
   std::vector<double> load(static_cast<size_t>(G));
   // g < 0: heaviest first across all heads; g >= 0: head by head, g tail heads
   auto balance = [&](int g) {
@@ -333,101 +314,12 @@ int causal_order(int BH, int n_qtiles, int n_pairs, int G, double kv_head_bytes)
   return best >= balance(-1) - 0.08 ? best_g : -1;
 }
 
-// Per-CTA lists for a causal launch in item order `order` on G CTAs: each
-// item, in launch order, goes to the CTA with the smallest estimated load so
-// far (ties: the lower CTA), and keeps its place in that CTA's list.
-// Returns the lists' balance (mean load / largest), or 0 when the launch does
-// not fit the list form.
-double build_lists(int BH, int n_qtiles, int n_pairs, int G, int order, fa::SchedList &out) {
-  const int64_t n = static_cast<int64_t>(BH) * n_pairs;
-  if (n <= 0 || n > fa::kSchedMaxItems || G < 1 || G > fa::kSchedMaxCtas) return 0.0;
-  const std::vector<double> w = causal_item_loads(n_qtiles, n_pairs);
-  const int64_t first = order < 0 ? 0 : static_cast<int64_t>(BH - order) * n_pairs;
-  typedef std::pair<double, int> Slot;  // (load, CTA)
-  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-  for (int c = 0; c < G; ++c) heap.push(Slot(0.0, c));
-  std::vector<int> cta(static_cast<size_t>(n));
-  std::vector<int> count(static_cast<size_t>(G), 0);
-  double total = 0.0;
-  for (int64_t i = 0; i < n; ++i) {
-    int level;
-    if (order < 0) level = static_cast<int>(i / BH);
-    else if (i < first) level = static_cast<int>(i % n_pairs);
-    else level = static_cast<int>((i - first) / order);
-    const Slot s = heap.top();
-    heap.pop();
-    heap.push(Slot(s.first + w[static_cast<size_t>(level)], s.second));
-    cta[static_cast<size_t>(i)] = s.second;
-    ++count[static_cast<size_t>(s.second)];
-    total += w[static_cast<size_t>(level)];
-  }
-  double mx = 0.0;
-  while (!heap.empty()) {
-    mx = std::max(mx, heap.top().first);
-    heap.pop();
-  }
-  out.off[0] = 0;
-  for (int c = 0; c < G; ++c)
-    out.off[c + 1] = static_cast<uint16_t>(out.off[c] + count[static_cast<size_t>(c)]);
-  std::vector<int> fill(out.off, out.off + G);
-  for (int64_t i = 0; i < n; ++i)
-    out.item[fill[static_cast<size_t>(cta[static_cast<size_t>(i)])]++] = static_cast<uint16_t>(i);
-  return total / G / mx;
-}
-
-// Balance of the static rounds (round r: CTA b takes item r*G + b, or
-// r*G + G-1-b on odd rounds) in item order `order`, the model of
-// causal_order.
-double rounds_balance(int BH, int n_qtiles, int n_pairs, int G, int order) {
-  const int64_t n = static_cast<int64_t>(BH) * n_pairs;
-  const std::vector<double> w = causal_item_loads(n_qtiles, n_pairs);
-  std::vector<double> load(static_cast<size_t>(G), 0.0);
-  const int64_t first = order < 0 ? 0 : static_cast<int64_t>(BH - order) * n_pairs;
-  double total = 0.0;
-  for (int64_t i = 0; i < n; ++i) {
-    int level;
-    if (order < 0) level = static_cast<int>(i / BH);
-    else if (i < first) level = static_cast<int>(i % n_pairs);
-    else level = static_cast<int>((i - first) / order);
-    const int64_t r = i / G, off = i % G;
-    load[static_cast<size_t>((r & 1) ? G - 1 - off : off)] += w[static_cast<size_t>(level)];
-    total += w[static_cast<size_t>(level)];
-  }
-  double mx = 0.0;
-  for (double x : load) mx = std::max(mx, x);
-  return total / G / mx;
-}
-
-// The plan of a causal launch, computed once per (B*H, Q tiles) and cached.
-CausalPlan causal_plan(DeviceState &ds, int BH, int n_qtiles, int D) {
-  const int n_pairs = (n_qtiles + 1) / 2;
-  const double kv_bytes = 2.0 * BH * static_cast<double>(n_qtiles) * 128.0 * D * 2.0;
-  if (kv_bytes <= 64.0 * 1024 * 1024) return CausalPlan();  // L2 holds K/V: heaviest first
-  const uint64_t key = (static_cast<uint64_t>(BH) << 32) | static_cast<uint32_t>(n_qtiles);
-  std::lock_guard<std::mutex> lock(ds.order_mu);
-  auto hit = ds.order_cache.find(key);
-  if (hit != ds.order_cache.end()) return hit->second;
-  if (ds.order_cache.size() >= 4096) ds.order_cache.clear();  // bounded
-  CausalPlan plan;
-  plan.order = causal_order(BH, n_qtiles, n_pairs, ds.sm_count, kv_bytes / BH);
-  if (plan.order >= 0) {
-    const int64_t n = static_cast<int64_t>(BH) * n_pairs;
-    const int G = static_cast<int>(std::min<int64_t>(n, ds.sm_count));
-    auto list = std::make_shared<fa::SchedList>();
-    const double b = build_lists(BH, n_qtiles, n_pairs, G, plan.order, *list);
-    if (b > rounds_balance(BH, n_qtiles, n_pairs, G, plan.order) + 0.005) plan.list = list;
-  }
-  ds.order_cache.emplace(key, plan);
-  return plan;
-}
-
-template <int D, bool BF16, int STAGES, int EXPSPLIT, bool STATS, bool LIST>
+template <int D, bool BF16, int STAGES, int EXPSPLIT, bool STATS>
 int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *v, void *o,
            float *lse, int64_t BH, int64_t N, int causal, float scale, float thr, bool noalloc,
-           unsigned long long *stats, int order, const fa::SchedList *list, cudaStream_t stream) {
+           unsigned long long *stats, int order, cudaStream_t stream) {
   using C = fa::Cfg<D, BF16, STAGES, EXPSPLIT, STATS>;
-  auto kernel = fa::fa_fwd_kernel<D, BF16, STAGES, EXPSPLIT, STATS, LIST>;
-  if (LIST) slot += kMaxVariants;  // the list instance has attributes of its own
+  auto kernel = fa::fa_fwd_kernel<D, BF16, STAGES, EXPSPLIT, STATS>;
   std::call_once(ds.attr_once[slot], [&] {
     cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -451,9 +343,26 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
   p.n_pairs = (p.n_qtiles + 1) / 2;
   p.n_items = p.BH * p.n_pairs;
   p.causal = causal ? 1 : 0;
-  // causal item order, as the caller resolved it (causal_plan or an override)
-  p.causal_head_major = causal && order >= 0 ? 1 : 0;
-  p.causal_tail_heads = causal && order >= 0 ? order : 0;
+  // K and V of all heads beyond 64 MiB: L2 (126 MB) no longer holds them
+  const double kv_bytes = 2.0 * static_cast<double>(BH) * static_cast<double>(N) * D * 2.0;
+  p.causal_head_major = 0;
+  p.causal_tail_heads = 0;
+  if (causal && kv_bytes > 64.0 * 1024 * 1024) {
+    const uint64_t key = (static_cast<uint64_t>(p.BH) << 32) | static_cast<uint32_t>(p.n_qtiles);
+    std::lock_guard<std::mutex> lock(ds.order_mu);
+    auto hit = ds.order_cache.find(key);
+    if (hit == ds.order_cache.end()) {
+      if (ds.order_cache.size() >= 4096) ds.order_cache.clear();  // bounded
+      const int g = causal_order(p.BH, p.n_qtiles, p.n_pairs, ds.sm_count, kv_bytes / BH);
+      hit = ds.order_cache.emplace(key, g).first;
+    }
+    p.causal_head_major = hit->second >= 0 ? 1 : 0;
+    p.causal_tail_heads = hit->second >= 0 ? hit->second : 0;
+  }
+  if (causal && order != kOrderAuto) {  // fa_fwd_variant's override
+    p.causal_head_major = order >= 0 ? 1 : 0;
+    p.causal_tail_heads = order >= 0 ? order : 0;
+  }
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.rescale_thr = thr;
   p.stats = stats;
@@ -528,9 +437,7 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
   }
 
   const int grid = p.n_units < ds.sm_count ? p.n_units : ds.sm_count;
-  fa::SchedT<LIST> sch;
-  if constexpr (LIST) sch = *list;  // built by the caller for `grid` CTAs
-  kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p, sch);
+  kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
   cudaError_t e = cudaGetLastError();
   if (scratch != nullptr) cudaFreeAsync(scratch, stream);
   if (e != cudaSuccess) {
@@ -547,25 +454,21 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
 // for tuning and measurement.
 typedef int (*LaunchFn)(DeviceState &, int, const void *, const void *, const void *, void *,
                         float *, int64_t, int64_t, int, float, float, bool,
-                        unsigned long long *, int, const fa::SchedList *, cudaStream_t);
+                        unsigned long long *, int, cudaStream_t);
 struct Variant {
   int d;
   bool bf16;
   int stages;     // K/V ring slots (the resolved count)
   int exp_split;  // every exp_split-th pair of exponentials on the FMA pipes (0: none)
   bool stats;
-  LaunchFn fn;       // static rounds
-  LaunchFn fn_list;  // per-CTA lists (causal launches; the defaults only), or null
+  LaunchFn fn;
 };
-#define FA_V(DD, BB, ST, SP, STATS)                                                   \
-  Variant{DD, BB, fa::Cfg<DD, BB, ST, SP, STATS>::kStages, SP, STATS,                 \
-          launch<DD, BB, ST, SP, STATS, false>, nullptr}
-#define FA_VL(DD, BB)                                                                 \
-  Variant{DD, BB, fa::Cfg<DD, BB, 0, 0, false>::kStages, 0, false,                    \
-          launch<DD, BB, 0, 0, false, false>, launch<DD, BB, 0, 0, false, true>}
+#define FA_V(DD, BB, ST, SP, STATS) \
+  Variant{DD, BB, fa::Cfg<DD, BB, ST, SP, STATS>::kStages, SP, STATS, launch<DD, BB, ST, SP, STATS>}
 const Variant kVariants[] = {
     // defaults (product entry points)
-    FA_VL(64, true), FA_VL(64, false), FA_VL(128, true), FA_VL(128, false),
+    FA_V(64, true, 0, 0, false), FA_V(64, false, 0, 0, false),
+    FA_V(128, true, 0, 0, false), FA_V(128, false, 0, 0, false),
     // d = 128 ring depths and exp splits
     FA_V(128, true, 2, 0, false), FA_V(128, true, 3, 0, false),
     FA_V(128, true, 0, 4, false), FA_V(128, true, 0, 2, false),
@@ -577,7 +480,6 @@ const Variant kVariants[] = {
     FA_V(64, true, 0, 0, true), FA_V(128, true, 0, 0, true), FA_V(128, false, 0, 0, true),
 };
 #undef FA_V
-#undef FA_VL
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 static_assert(kNumVariants <= kMaxVariants, "more variants than per-device attribute slots");
 
@@ -596,8 +498,7 @@ int find_variant(int d, bool bf16, int stages, int exp_split, bool stats) {
 int fwd_common(bool bf16, const void *q, const void *k, const void *v, void *o, float *lse,
                int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
                float thr, fa_stream_t stream, bool noalloc = false, int variant = -1,
-               unsigned long long *stats = nullptr, int order = kOrderAuto,
-               int schedule = kScheduleAuto) {
+               unsigned long long *stats = nullptr, int order = kOrderAuto) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_HEADDIM;
@@ -620,41 +521,13 @@ int fwd_common(bool bf16, const void *q, const void *k, const void *v, void *o, 
   if (variant < 0) variant = (d == 64 ? 0 : 2) + (bf16 ? 0 : 1);  // the default variants
   if (kVariants[variant].d != d || kVariants[variant].bf16 != bf16) return FA_ERR_OPTION;
   if (order != kOrderAuto && (order < -1 || order > BH)) return FA_ERR_OPTION;
-  if (schedule < kScheduleAuto || schedule > kScheduleLists) return FA_ERR_OPTION;
-  const Variant &var = kVariants[variant];
-  if (schedule == kScheduleLists && (!causal || var.fn_list == nullptr)) return FA_ERR_OPTION;
 
   DeviceState *ds = nullptr;
   int rc = device_state(&ds);
   if (rc != FA_OK) return rc;
   if (!noalloc) ensure_pool(*ds, ds->dev);
-  // causal: the item order and, where they balance better, per-CTA lists
-  int eff_order = -1;
-  std::shared_ptr<fa::SchedList> list;
-  if (causal) {
-    const int n_qtiles = static_cast<int>((N + 127) / 128);
-    const CausalPlan plan = causal_plan(*ds, static_cast<int>(BH), n_qtiles, static_cast<int>(d));
-    eff_order = order != kOrderAuto ? order : plan.order;
-    if (schedule == kScheduleRounds) {
-      // static rounds: no list
-    } else if (schedule == kScheduleLists) {
-      if (order == kOrderAuto && plan.list) {
-        list = plan.list;
-      } else {  // built for this call (tuning only)
-        const int n_pairs = (n_qtiles + 1) / 2;
-        const int64_t n = BH * n_pairs;
-        const int G = static_cast<int>(std::min<int64_t>(n, ds->sm_count));
-        list = std::make_shared<fa::SchedList>();
-        if (build_lists(static_cast<int>(BH), n_qtiles, n_pairs, G, eff_order, *list) <= 0.0)
-          return FA_ERR_OPTION;
-      }
-    } else if (schedule == kScheduleAuto && order == kOrderAuto) {
-      list = plan.list;
-    }
-  }
-  LaunchFn fn = (list && var.fn_list) ? var.fn_list : var.fn;
-  return fn(*ds, variant, q, k, v, o, lse, BH, N, causal, scale, thr, noalloc, stats, eff_order,
-            fn == var.fn_list ? list.get() : nullptr, static_cast<cudaStream_t>(stream));
+  return kVariants[variant].fn(*ds, variant, q, k, v, o, lse, BH, N, causal, scale, thr, noalloc,
+                               stats, order, static_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------- backward
@@ -769,13 +642,13 @@ int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *
 int fa_fwd_variant(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
                    int64_t H, int64_t N, int64_t d, int causal, float scale, int fp16,
                    float rescale_threshold, int stages, int exp_split, int causal_order,
-                   int schedule, unsigned long long *stats, fa_stream_t stream) {
+                   unsigned long long *stats, fa_stream_t stream) {
   if (d != 64 && d != 128) return d < 1 ? FA_ERR_SHAPE : FA_ERR_HEADDIM;
   const int idx = find_variant(static_cast<int>(d), fp16 == 0, stages, exp_split, stats != nullptr);
   if (idx < 0) return FA_ERR_OPTION;
   if (stats != nullptr && (reinterpret_cast<uintptr_t>(stats) & 7u)) return FA_ERR_ALIGN;
   return fwd_common(fp16 == 0, q, k, v, o, lse, B, H, N, d, causal, scale, rescale_threshold,
-                    stream, /*noalloc=*/false, idx, stats, causal_order, schedule);
+                    stream, /*noalloc=*/false, idx, stats, causal_order);
 }
 
 int fa_bwd_workspace_size(int64_t B, int64_t H, int64_t N, int64_t d, size_t *bytes) {
@@ -831,24 +704,15 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
 
 int fa_variant_count(void) { return kNumVariants; }
 
-int fa_causal_order(int64_t B, int64_t H, int64_t N, int64_t d, int sm_count, int *lists) {
+int fa_causal_order(int64_t B, int64_t H, int64_t N, int64_t d, int sm_count) {
   if (B < 1 || H < 1 || N < 1 || N > FA_MAX_N || sm_count < 1) return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_HEADDIM;
   const int64_t BH = B * H;
   if (BH * ((N + 255) / 256) > INT32_MAX / 2) return FA_ERR_SHAPE;
   const int n_qtiles = static_cast<int>((N + 127) / 128), n_pairs = (n_qtiles + 1) / 2;
   const double kv_bytes = 2.0 * static_cast<double>(BH) * static_cast<double>(N) * d * 2.0;
-  if (lists) *lists = 0;
   if (kv_bytes <= 64.0 * 1024 * 1024) return -1;
-  const int order = causal_order(static_cast<int>(BH), n_qtiles, n_pairs, sm_count, kv_bytes / BH);
-  if (lists && order >= 0) {
-    const int64_t n = BH * n_pairs;
-    const int G = static_cast<int>(std::min<int64_t>(n, sm_count));
-    fa::SchedList tmp;
-    const double b = build_lists(static_cast<int>(BH), n_qtiles, n_pairs, G, order, tmp);
-    *lists = b > rounds_balance(static_cast<int>(BH), n_qtiles, n_pairs, G, order) + 0.005 ? 1 : 0;
-  }
-  return order;
+  return causal_order(static_cast<int>(BH), n_qtiles, n_pairs, sm_count, kv_bytes / BH);
 }
 
 int fa_variant_info(int index, int *d, int *fp16, int *stages, int *exp_split, int *stats) {

@@ -50,7 +50,6 @@
 #pragma once
 
 #include <cuda_bf16.h>
-#include <type_traits>
 #include <cuda_fp16.h>
 
 #include "ptx.cuh"
@@ -97,20 +96,6 @@ struct Params {
 // and 8 at d = 64), EXPSPLIT = every EXPSPLIT-th pair of the softmax's
 // exponentials is evaluated on the FMA pipes (exp2_poly2) instead of the
 // special-function unit (0: none), STATS = count rescales (Params::stats).
-// Per-CTA lists of causal work items, built by the host (a greedy list
-// schedule over the chosen item order: each item to the CTA whose estimated
-// load is smallest) and passed as a kernel parameter, so they cost no
-// device memory.  CTA c takes item[off[c]] .. item[off[c+1] - 1] in turn.
-constexpr int kSchedMaxCtas = 160;
-constexpr int kSchedMaxItems = 3904;
-struct SchedList {
-  uint16_t off[kSchedMaxCtas + 1];
-  uint16_t item[kSchedMaxItems];
-};
-struct SchedNone {};
-template <bool LIST>
-using SchedT = typename std::conditional<LIST, SchedList, SchedNone>::type;
-
 template <int D, bool BF16, int STAGES = 0, int EXPSPLIT = 0, bool STATS = false>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
@@ -362,30 +347,11 @@ __device__ __forceinline__ void store_rows(uint4 (&v)[NC], uint8_t *row0, size_t
   }
 }
 
-template <int D, bool BF16, int STAGES = 0, int EXPSPLIT = 0, bool STATS = false, bool LIST = false>
+template <int D, bool BF16, int STAGES = 0, int EXPSPLIT = 0, bool STATS = false>
 __global__ void __launch_bounds__(Cfg<D, BF16, STAGES, EXPSPLIT, STATS>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const Params p,
-                  const __grid_constant__ SchedT<LIST> sch) {
+                  const __grid_constant__ CUtensorMap tm_v, const Params p) {
   using C = Cfg<D, BF16, STAGES, EXPSPLIT, STATS>;
-  // This CTA's work: LIST, its list from the host; otherwise the static
-  // rounds (round r: unit round_item(r)).  Both are read from the kernel's
-  // parameters each time (nothing held in registers across the loops).
-  // unit_at returns -1 for a round with no unit for this CTA.
-  auto more_rounds = [&](int r) -> bool {
-    if constexpr (LIST) {
-      return r < sch.off[blockIdx.x + 1] - sch.off[blockIdx.x];
-    } else {
-      return r * static_cast<int>(gridDim.x) < p.n_units;
-    }
-  };
-  auto unit_at = [&](int r) -> int {
-    if constexpr (LIST) {
-      return sch.item[sch.off[blockIdx.x] + r];
-    } else {
-      return round_item(r, p);
-    }
-  };
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte-swizzled tiles.
   const uint32_t raw = smem_u32(smem_raw);
@@ -450,8 +416,8 @@ __global__ void __launch_bounds__(Cfg<D, BF16, STAGES, EXPSPLIT, STATS>::kThread
       uint32_t slot = 0, phase = 0, q_phase[2] = {0, 0};
       uint32_t kv_loads = 0, q_loads[2] = {0, 0};
       bool ok = true;
-      for (int round = 0; ok && more_rounds(round); ++round) {
-        const int item = unit_at(round);
+      for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_units; ++round) {
+        const int item = round_item(round, p);
         if (item < 0) continue;
         const Item it = decode_unit(item, p);
         // Each Q tile's buffer is released by its own last S MMA of the
@@ -539,8 +505,8 @@ __global__ void __launch_bounds__(Cfg<D, BF16, STAGES, EXPSPLIT, STATS>::kThread
       // of a K slot) falls right after PV0's MMAs are queued: between the end
       // of S1's issue and the start of PV0's there is then only one commit
       // and one wait, and the tensor core's short queue does not run dry.
-      for (int round = 0; ok && more_rounds(round); ++round) {
-        const int item = unit_at(round);
+      for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_units; ++round) {
+        const int item = round_item(round, p);
         if (item < 0) continue;
         const Item it = decode_unit(item, p);
         const int n_max = it.n0 > it.n1 ? it.n0 : it.n1;
@@ -666,8 +632,8 @@ __global__ void __launch_bounds__(Cfg<D, BF16, STAGES, EXPSPLIT, STATS>::kThread
         mma_commit_if(leader, bar(C::kPVDone + t));
         return true;
       };
-      for (int round = 0; ok && more_rounds(round); ++round) {
-        const int item = unit_at(round);
+      for (int round = 0; ok && round * static_cast<int>(gridDim.x) < p.n_units; ++round) {
+        const int item = round_item(round, p);
         if (item < 0) continue;
         const Item it = decode_unit(item, p);
         const int n0 = it.n0, n1 = it.n1;  // n1: 0 (no tile 1), n0 or n0 + 1
@@ -812,8 +778,8 @@ __global__ void __launch_bounds__(Cfg<D, BF16, STAGES, EXPSPLIT, STATS>::kThread
     // keeps walking the same sequence of blocks, doing no work but taking
     // part in every pair barrier, so its partner can never be left waiting.
     bool ok = true;
-    for (int round = 0; more_rounds(round); ++round) {
-      const int item = unit_at(round);
+    for (int round = 0; round * static_cast<int>(gridDim.x) < p.n_units; ++round) {
+      const int item = round_item(round, p);
       if (item < 0) continue;
       const Item it = decode_unit(item, p);
       const int n = t ? it.n1 : it.n0;  // this tile's K/V blocks (0: no tile 1)

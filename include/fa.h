@@ -85,10 +85,6 @@ typedef void *fa_stream_t;
 
 /* fa_fwd_variant: let the library choose the causal item order. */
 #define FA_ORDER_AUTO (-2)
-/* fa_fwd_variant: how causal CTAs find their items. */
-#define FA_SCHEDULE_AUTO 0
-#define FA_SCHEDULE_ROUNDS 1
-#define FA_SCHEDULE_LISTS 2
 
 /* Rescale threshold used by fa_fwd and fa_fwd_fp16, in log2 units of the
  * scaled logits (see fa_fwd_ex). */
@@ -198,12 +194,6 @@ int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *
  *   causal_order : FA_ORDER_AUTO (the library's choice, see
  *               fa_causal_order), or an order to force on causal launches:
  *               -1 or g in [0, B*H] with fa_causal_order's meaning
- *   schedule  : how a causal launch's CTAs find their items:
- *               FA_SCHEDULE_AUTO (the library's choice), FA_SCHEDULE_ROUNDS
- *               (static rounds) or FA_SCHEDULE_LISTS (per-CTA lists, built on
- *               the host and passed as a kernel parameter; only for the
- *               default ring depth without exp split or counters, causal,
- *               and at most 3904 items on at most 160 CTAs)
  *   stats     : NULL, or a DEVICE array of 4 unsigned 64-bit counters that
  *               the kernel adds to (the caller zeroes it): [0] (row, K/V
  *               block) pairs after a tile's first block where the running
@@ -219,7 +209,7 @@ int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *
 int fa_fwd_variant(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
                    int64_t H, int64_t N, int64_t d, int causal, float scale, int fp16,
                    float rescale_threshold, int stages, int exp_split, int causal_order,
-                   int schedule, unsigned long long *stats, fa_stream_t stream);
+                   unsigned long long *stats, fa_stream_t stream);
 int fa_variant_count(void);
 int fa_variant_info(int index, int *d, int *fp16, int *stages, int *exp_split, int *stats);
 
@@ -231,12 +221,9 @@ int fa_variant_info(int index, int *d, int *fp16, int *stages, int *exp_split, i
  *          all heads total at most 64 MiB);
  *   g >= 0 head by head, heaviest pair first within a head, with the last
  *          g heads taken together, heaviest pair first across them.
- * *lists (if not NULL) is set to 1 when the CTAs take those items from
- * per-CTA lists (a greedy list schedule that balances better than the
- * static rounds), else 0.
  * FA_ERR_SHAPE / FA_ERR_HEADDIM on bad arguments.  For tests and tuning.
  */
-int fa_causal_order(int64_t B, int64_t H, int64_t N, int64_t d, int sm_count, int *lists);
+int fa_causal_order(int64_t B, int64_t H, int64_t N, int64_t d, int sm_count);
 
 /*
  * fa_bwd -- gradients of the attention forward (the backward pass).

@@ -150,14 +150,13 @@ def test_selftest_argument_errors(lib):
 def test_fa_fwd_variant_argument_errors(lib):
     """Variants that are not built, and bad arguments, are refused before
     any device call; every built variant is listed with a valid shape."""
-    def var(stages=0, exp_split=0, stats=None, order=fa.FA_ORDER_AUTO,
-            schedule=fa.FA_SCHEDULE_AUTO, **kw):
+    def var(stages=0, exp_split=0, stats=None, order=fa.FA_ORDER_AUTO, **kw):
         a = dict(q=Q, k=K, v=V, o=O, lse=L, B=1, H=1, N=128, d=128, causal=0, scale=0.125,
                  fp16=0, thr=8.0)
         a.update(kw)
         return lib.fa_fwd_variant(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"],
                                   a["N"], a["d"], a["causal"], a["scale"], a["fp16"], a["thr"],
-                                  stages, exp_split, order, schedule, stats, None)
+                                  stages, exp_split, order, stats, None)
     assert var(stages=5) == fa.FA_ERR_OPTION        # no room for five 32 KiB slots
     assert var(stages=7, d=64) == fa.FA_ERR_OPTION  # not built
     assert var(exp_split=3) == fa.FA_ERR_OPTION
@@ -170,10 +169,6 @@ def test_fa_fwd_variant_argument_errors(lib):
     assert var(stages=3, o=Q) == fa.FA_ERR_ALIAS
     assert var(order=-3) == fa.FA_ERR_OPTION
     assert var(order=2, B=1, H=1) == fa.FA_ERR_OPTION  # more tail heads than heads
-    assert var(schedule=3) == fa.FA_ERR_OPTION
-    assert var(schedule=-1) == fa.FA_ERR_OPTION
-    assert var(schedule=fa.FA_SCHEDULE_LISTS) == fa.FA_ERR_OPTION  # lists: causal only
-    assert var(schedule=fa.FA_SCHEDULE_LISTS, causal=1, stages=3) == fa.FA_ERR_OPTION
     vs = fa.variants()
     assert len(vs) == lib.fa_variant_count()
     assert vs[:4] == [dict(d=64, fp16=0, stages=8, exp_split=0, stats=0),

@@ -1,17 +1,13 @@
 """The host's choice of causal work-item order (no GPU needed).
 
 The library simulates, per shape, how the static rounds of its persistent
-grid load each SM under a few item orders, and picks one; then it builds
-per-CTA lists (each item, in launch order, to the CTA with the smallest
-load so far) and uses them where they balance better than the rounds.  This
-restates that cost model independently in Python -- an item of two Q tiles
-costs the larger tile's K/V blocks plus 1.3 blocks of restart; round r
-gives item r*G + b to CTA b, reversed on odd rounds -- and checks that
-fa_causal_order returns the order and the list decision the model prefers,
-over a spread of shapes and SM counts.
+grid load each SM under a few item orders, and picks one.  This restates
+that cost model independently in Python -- an item of two Q tiles costs the
+larger tile's K/V blocks plus 1.3 blocks of restart; round r gives item
+r*G + b to CTA b, reversed on odd rounds -- and checks that fa_causal_order
+returns the order the model prefers, over a spread of shapes and SM counts.
 """
 import ctypes
-import heapq
 
 import pytest
 
@@ -25,14 +21,9 @@ MIB = 1024 * 1024
 def order_fn():
     fa_build.build()
     f = fa.lib().fa_causal_order
-    f.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+    f.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int]
     f.restype = ctypes.c_int
-
-    def call(B, H, N, d, G):
-        lists = ctypes.c_int(-1)
-        order = f(B, H, N, d, G, ctypes.byref(lists))
-        return order, lists.value
-    return call
+    return f
 
 
 def item_levels(BH, P, g):
@@ -45,18 +36,12 @@ def item_levels(BH, P, g):
     return [i % P if i < first else (i - first) // g for i in range(BH * P)]
 
 
-def item_costs(T):
+def balance(BH, T, G, g):
     P = (T + 1) // 2
     cost = []
     for level in range(P):
         qt1 = 2 * (P - 1 - level) + 1
         cost.append((qt1 + 1 if qt1 < T else qt1) + 1.3)
-    return cost
-
-
-def balance(BH, T, G, g):
-    P = (T + 1) // 2
-    cost = item_costs(T)
     load = [0.0] * G
     for i, lv in enumerate(item_levels(BH, P, g)):
         r, off = divmod(i, G)
@@ -64,27 +49,12 @@ def balance(BH, T, G, g):
     return sum(load) / G / max(load)
 
 
-def list_balance(BH, T, G, g):
-    """Greedy list schedule: each item in launch order to the least-loaded
-    CTA (ties: the lower CTA)."""
-    P = (T + 1) // 2
-    cost = item_costs(T)
-    heap = [(0.0, c) for c in range(G)]
-    total = 0.0
-    for lv in item_levels(BH, P, g):
-        load, c = heapq.heappop(heap)
-        heapq.heappush(heap, (load + cost[lv], c))
-        total += cost[lv]
-    return total / G / max(x for x, _ in heap)
-
-
 def expected(B, H, N, d, G):
-    """(order, lists) the cost model prefers."""
     BH, T = B * H, (N + 127) // 128
     P = (T + 1) // 2
     kv_head = 2 * N * d * 2
     if BH * kv_head <= 64 * MIB or BH * P <= G or BH * P > 1 << 20:
-        return -1, 0
+        return -1
     best_g, best = 0, balance(BH, T, G, 0)
     for g in (2, 4, 6, 8, 12, 16, 24, 32):
         if g >= BH or g * kv_head > 96 * MIB:
@@ -92,11 +62,7 @@ def expected(B, H, N, d, G):
         b = balance(BH, T, G, g)
         if b > best + 1e-9:
             best_g, best = g, b
-    if best < balance(BH, T, G, None) - 0.08:
-        return -1, 0
-    n = BH * P
-    lists = int(n <= 3904 and G <= 160 and list_balance(BH, T, G, best_g) > best + 0.005)
-    return best_g, lists
+    return best_g if best >= balance(BH, T, G, None) - 0.08 else -1
 
 
 SHAPES = [(1, 32, 16384, 128), (8, 16, 4096, 128), (16, 32, 8192, 128), (8, 64, 1024, 64),
@@ -111,9 +77,7 @@ def test_causal_order_matches_the_cost_model(order_fn, B, H, N, d, G):
 
 
 def test_causal_order_argument_errors(order_fn):
-    assert order_fn(0, 1, 128, 128, 152)[0] == fa.FA_ERR_SHAPE
-    assert order_fn(1, 1, 128, 96, 152)[0] == fa.FA_ERR_HEADDIM
-    assert order_fn(1, 1, 128, 128, 0)[0] == fa.FA_ERR_SHAPE
-    # the long causal target shape: 12 tail heads, from per-CTA lists
-    assert order_fn(1, 32, 16384, 128, 152) == (12, 1)
-    assert order_fn(8, 16, 4096, 128, 152) == (32, 0)  # the rounds balance as well
+    assert order_fn(0, 1, 128, 128, 152) == fa.FA_ERR_SHAPE
+    assert order_fn(1, 1, 128, 96, 152) == fa.FA_ERR_HEADDIM
+    assert order_fn(1, 1, 128, 128, 0) == fa.FA_ERR_SHAPE
+    assert order_fn(1, 32, 16384, 128, 152) == 12  # the long causal target shape

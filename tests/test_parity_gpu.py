@@ -144,31 +144,21 @@ def test_parity_causal_head_by_head_order():
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
 
 
-TAIL_WINDOW_SHAPES = [(1, 32, 16384, 128), (8, 16, 4096, 128), (4, 48, 4096, 64),
-                      (1, 24, 16384, 128)]
-
-
-def _causal_plan(B, H, N, d):
-    import ctypes
-    f = fa().lib().fa_causal_order
-    f.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
-    f.restype = ctypes.c_int
-    lists = ctypes.c_int(0)
-    g = f(B, H, N, d, torch.cuda.get_device_properties(0).multi_processor_count,
-          ctypes.byref(lists))
-    return g, lists.value
+TAIL_WINDOW_SHAPES = [(1, 32, 16384, 128), (8, 16, 4096, 128), (4, 48, 4096, 64)]
 
 
 @pytest.mark.parametrize("B,H,N,d", TAIL_WINDOW_SHAPES,
                          ids=[f"b{b}h{h}n{n}d{d}" for b, h, n, d in TAIL_WINDOW_SHAPES])
 def test_parity_causal_tail_window_order(B, H, N, d):
     """Causal launches taken head by head with their last heads taken
-    together, from per-CTA lists where the host builds them (the host's
-    choice for these shapes on a 152-SM GB300): one seeded row of every
-    (head, Q tile) is checked against the oracle, so a work item that went
-    missing or to the wrong head cannot pass.  The static rounds and the
-    lists compute every item the same way, so both give the same bits."""
-    g, lists = _causal_plan(B, H, N, d)
+    together (the host's choice for these shapes on a 152-SM GB300): one
+    seeded row of every (head, Q tile) is checked against the oracle, so a
+    work item that went missing or to the wrong head cannot pass."""
+    import ctypes
+    f = fa().lib().fa_causal_order
+    f.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int]
+    f.restype = ctypes.c_int
+    g = f(B, H, N, d, torch.cuda.get_device_properties(0).multi_processor_count)
     q, k, v = make_qkv(B, H, N, d, torch.bfloat16, seed=4300 + N + H)
     o, lse = run_gpu(q, k, v, True)
     BH, tiles = B * H, N // 128
@@ -177,35 +167,8 @@ def test_parity_causal_tail_window_order(B, H, N, d):
                      for h in range(BH) for t in range(tiles)], dtype=np.int64)
     o_ref, lse_ref = oracle.attn_fwd(q, k, v, True, 1.0 / math.sqrt(d), rows=rows)
     assert_close(o.reshape(BH * N, d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref,
-                 f"causal {B},{H},{N},{d} order {g} lists {lists}")
+                 f"causal {B},{H},{N},{d} order {g}")
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
-    dev = torch.device("cuda")
-    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    for schedule in (fa().FA_SCHEDULE_ROUNDS, fa().FA_SCHEDULE_LISTS):
-        o2 = torch.empty_like(qd)
-        l2 = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        fa().fa_fwd_variant(qd, kd, vd, o2, l2, causal=True, schedule=schedule)
-        torch.cuda.synchronize()
-        assert fa().fa_get_status() == 0
-        assert np.array_equal(o2.float().cpu().numpy(), o) and np.array_equal(l2.cpu().numpy(), lse)
-
-
-def test_lists_with_forced_orders_bitwise():
-    """Per-CTA lists built for forced item orders (heaviest first across
-    heads, plain head by head) give the rounds' bits on a causal launch with
-    ragged last tiles."""
-    B, H, N, d = 2, 40, 3000, 64
-    dev = torch.device("cuda")
-    qd, kd, vd = (x.to(dev) for x in make_qkv(B, H, N, d, torch.bfloat16, seed=4400))
-    ref_o, ref_l = fa().forward(qd, kd, vd, causal=True)
-    for order in (-1, 0, 8):
-        o2 = torch.empty_like(qd)
-        l2 = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        fa().fa_fwd_variant(qd, kd, vd, o2, l2, causal=True, causal_order=order,
-                            schedule=fa().FA_SCHEDULE_LISTS)
-        torch.cuda.synchronize()
-        assert fa().fa_get_status() == 0
-        assert torch.equal(o2, ref_o) and torch.equal(l2, ref_l)
 
 
 def test_uniform_attention_q_zero():
