@@ -182,3 +182,44 @@ def test_bwd_cuda_graph_capture_replays():
         assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
         assert torch.allclose(dq.float(), ref[0].float(), rtol=1e-2, atol=1e-3)
     assert fa().fa_get_status() == 0
+
+
+def _random_bwd_cases(n, seed, n_lo=1, n_hi=1500):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        d = int(rng.choice([64, 128]))
+        N = int(rng.integers(n_lo, n_hi))
+        B = int(rng.integers(1, 3))
+        H = int(rng.integers(1, 4))
+        causal = bool(rng.integers(0, 2))
+        dtype = torch.bfloat16 if rng.integers(0, 2) else torch.float16
+        cases.append((B, H, N, d, causal, dtype))
+    return cases
+
+
+RANDOM_BWD = _random_bwd_cases(16, seed=3030)
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,dtype", RANDOM_BWD,
+                         ids=[f"b{b}h{h}n{n}d{d}-{'c' if c else 'f'}-{str(t)[6:]}"
+                              for b, h, n, d, c, t in RANDOM_BWD])
+def test_bwd_parity_random_shapes(B, H, N, d, causal, dtype):
+    """Seeded random shapes: any N up to 1500 (ragged last tiles, a single
+    partial tile), both head dims, masks and dtypes, full tensors."""
+    q, k, v, do = grad_inputs(B, H, N, d, dtype, seed=7000 + N + d + H)
+    got = run_gpu_bwd(q, k, v, do, causal)
+    ref = oracle.attn_bwd(q, k, v, do, causal, 1.0 / math.sqrt(d))
+    assert_grads_close(got, ref, f"{B},{H},{N},{d},causal={causal},{dtype}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_bwd_parity_long_sequence(causal, d):
+    """N = 8192 (64 key blocks per query block, 64 query blocks per key
+    block: the dQ accumulators take 64 additions per element), two heads,
+    every row against the oracle."""
+    q, k, v, do = grad_inputs(1, 2, 8192, d, torch.bfloat16, seed=7100 + d)
+    got = run_gpu_bwd(q, k, v, do, causal)
+    ref = oracle.attn_bwd(q, k, v, do, causal, 1.0 / math.sqrt(d))
+    assert_grads_close(got, ref, f"[1,2,8192,{d}] causal={causal}")
