@@ -19,7 +19,8 @@ Sources of each fact:
  - adding a vector to every key leaves O, hence every gradient, unchanged;
  - linearity of the gradients in dO;
  - torch autograd of a library softmax in fp64 (a special case that
-   reduces to a library routine).
+   reduces to a library routine);
+ - a two-query, two-key case derived by hand (tests/golden/two_key_backward.txt).
 """
 from __future__ import annotations
 
@@ -151,6 +152,26 @@ def check_torch_autograd(lib=None):
             assert np.max(np.abs(ours - ref.numpy())) <= 1e-12
 
 
-ALL_CHECKS = [check_finite_differences, check_constant_v, check_single_key,
+def check_two_key_golden(lib=None):
+    """The hand derivation of tests/golden/two_key_backward.txt (two
+    queries, two keys, d = 1), both masks."""
+    import os
+    vals = {}
+    with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                           "two_key_backward.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                key, *nums = line.split()
+                vals[key] = np.array([float(x) for x in nums])
+    q, k, v, do = (vals[n].reshape(1, 1, 2, 1) for n in ("q", "k", "v", "dout"))
+    for causal, tag in ((False, "noncausal"), (True, "causal")):
+        dq, dk, dv = _grads(q, k, v, do, causal, 1.0, lib)
+        assert np.max(np.abs(dq.reshape(-1) - vals["dq_" + tag])) <= TOL, (tag, dq)
+        assert np.max(np.abs(dk.reshape(-1) - vals["dk_" + tag])) <= TOL, (tag, dk)
+        assert np.max(np.abs(dv.reshape(-1) - vals["dv_" + tag])) <= TOL, (tag, dv)
+
+
+ALL_CHECKS = [check_two_key_golden, check_finite_differences, check_constant_v, check_single_key,
               check_q_zero_closed_form, check_dk_sums_to_zero, check_key_shift_invariance,
               check_linear_in_dout, check_torch_autograd]
