@@ -70,6 +70,9 @@ def _bind(path: str):
         lib.oracle_attn_bwd.argtypes = [P, P, P, P, I64, I64, I64, I64, ctypes.c_int,
                                         ctypes.c_double, P, P, P, ctypes.c_int]
         lib.oracle_attn_bwd.restype = ctypes.c_int
+        lib.oracle_attn_bwd_dq_rows.argtypes = [P, P, P, P, I64, I64, I64, I64, ctypes.c_int,
+                                                ctypes.c_double, P, I64, P, ctypes.c_int]
+        lib.oracle_attn_bwd_dq_rows.restype = ctypes.c_int
     return lib
 
 
@@ -147,6 +150,25 @@ def attn_bwd(q, k, v, dout, causal: bool, scale: float, nthreads: int | None = N
     if rc != 0:
         raise RuntimeError(f"oracle_attn_bwd failed with code {rc}")
     return dq, dk, dv
+
+
+def attn_bwd_dq_rows(q, k, v, dout, causal: bool, scale: float, rows,
+                     nthreads: int | None = None, lib=None):
+    """dQ [len(rows), d] fp64 of sum(dout * O) for the listed flat query rows
+    (b*H + h)*N + i: each needs only its own row of probabilities."""
+    q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    if q.ndim != 4 or any(x.shape != q.shape for x in (k, v, dout)):
+        raise ValueError("q, k, v, dout must share one [B, H, N, d] shape")
+    B, H, N, d = q.shape
+    rows_arr = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1)
+    dq = np.empty((rows_arr.size, d), dtype=np.float64)
+    rc = (lib or _load()).oracle_attn_bwd_dq_rows(
+        q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, B, H, N, d,
+        int(bool(causal)), float(scale), rows_arr.ctypes.data, rows_arr.size, dq.ctypes.data,
+        int(nthreads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_bwd_dq_rows failed with code {rc}")
+    return dq
 
 
 def attn_probs(q, k, causal: bool, scale: float, lib=None) -> np.ndarray:

@@ -169,3 +169,125 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v, const dou
     free(tids);
     return rc;
 }
+
+/*
+ * dQ only, for a list of query rows (flat ids (b*H + h)*N + i): each row's
+ * gradient needs only that row's probabilities, so large shapes can be
+ * checked on samples.  The same chain rule as oracle_attn_bwd, row by row:
+ * p_ij from the three-pass softmax, dp_ij = dO_i . v_j, r_i = sum_j p_ij dp_ij,
+ * dq_i = scale * sum_j p_ij (dp_ij - r_i) k_j.  dq is [nrows, d].
+ * Rows are split over nthreads POSIX threads.
+ */
+typedef struct {
+    const double *q, *k, *v, *dout;
+    int64_t N, d;
+    int causal;
+    double scale;
+    const int64_t *rows;
+    int64_t begin, end;
+    double *dq;
+    int status;
+} dq_job;
+
+static void *run_dq_job(void *arg)
+{
+    dq_job *jb = (dq_job *)arg;
+    const int64_t N = jb->N, d = jb->d;
+    double *s = (double *)malloc(sizeof(double) * 2 * (size_t)N);
+    if (!s) {
+        jb->status = -2;
+        return NULL;
+    }
+    double *dp = s + N;
+    for (int64_t r = jb->begin; r < jb->end; ++r) {
+        const int64_t flat = jb->rows[r], bh = flat / N, i = flat % N;
+        const double *qi = jb->q + flat * d, *doi = jb->dout + flat * d;
+        const double *K = jb->k + bh * N * d, *V = jb->v + bh * N * d;
+        const int64_t nvis = jb->causal ? i + 1 : N;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < nvis; ++j) {
+            double dot = 0.0;
+            for (int64_t c = 0; c < d; ++c)
+                dot += qi[c] * K[j * d + c];
+            s[j] = jb->scale * dot;
+            if (s[j] > m)
+                m = s[j];
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < nvis; ++j)
+            l += exp(s[j] - m);
+        double rr = 0.0;
+        for (int64_t j = 0; j < nvis; ++j) {
+            double dot = 0.0;
+            for (int64_t c = 0; c < d; ++c)
+                dot += doi[c] * V[j * d + c];
+            dp[j] = dot;
+            rr += exp(s[j] - m) / l * dot;
+        }
+        double *out = jb->dq + r * d;
+        for (int64_t c = 0; c < d; ++c)
+            out[c] = 0.0;
+        for (int64_t j = 0; j < nvis; ++j) {
+            const double ds = exp(s[j] - m) / l * (dp[j] - rr);
+            for (int64_t c = 0; c < d; ++c)
+                out[c] += jb->scale * ds * K[j * d + c];
+        }
+    }
+    free(s);
+    jb->status = 0;
+    return NULL;
+}
+
+int oracle_attn_bwd_dq_rows(const double *q, const double *k, const double *v,
+                            const double *dout, int64_t B, int64_t H, int64_t N, int64_t d,
+                            int causal, double scale, const int64_t *rows, int64_t nrows,
+                            double *dq, int nthreads)
+{
+    if (!q || !k || !v || !dout || !rows || !dq || B <= 0 || H <= 0 || N <= 0 || d <= 0 ||
+        nrows < 0)
+        return -1;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= B * H * N)
+            return -1;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > nrows)
+        nthreads = nrows > 0 ? (int)nrows : 1;
+    dq_job *jobs = (dq_job *)calloc((size_t)nthreads, sizeof(dq_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tids) {
+        free(jobs);
+        free(tids);
+        return -2;
+    }
+    int rc = 0, started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        dq_job *jb = &jobs[t];
+        jb->q = q; jb->k = k; jb->v = v; jb->dout = dout;
+        jb->N = N; jb->d = d;
+        jb->causal = causal; jb->scale = scale;
+        jb->rows = rows;
+        jb->begin = nrows * t / nthreads;
+        jb->end = nrows * (t + 1) / nthreads;
+        jb->dq = dq;
+        jb->status = -3;
+        if (t == 0)
+            continue;
+        if (pthread_create(&tids[t], NULL, run_dq_job, jb) != 0) {
+            rc = -3;
+            break;
+        }
+        started = t;
+    }
+    if (rc == 0)
+        run_dq_job(&jobs[0]);
+    for (int t = 1; t <= started; ++t)
+        pthread_join(tids[t], NULL);
+    if (rc == 0)
+        for (int t = 0; t < nthreads; ++t)
+            if (jobs[t].status != 0)
+                rc = jobs[t].status;
+    free(jobs);
+    free(tids);
+    return rc;
+}

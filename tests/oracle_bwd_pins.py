@@ -172,6 +172,29 @@ def check_two_key_golden(lib=None):
         assert np.max(np.abs(dv.reshape(-1) - vals["dv_" + tag])) <= TOL, (tag, dv)
 
 
-ALL_CHECKS = [check_two_key_golden, check_finite_differences, check_constant_v, check_single_key,
+def check_dq_rows_finite_differences(lib=None):
+    """The row-sampled dQ against central differences of the forward
+    oracle's L = sum(dO * O), for a few rows of a small case (both masks)."""
+    q, k, v = rand_qkv(1, 2, 7, 3, 47, k_mult=1.5)
+    do = np.random.default_rng(48).standard_normal(q.shape)
+    rows = np.array([0, 3, 6, 7, 13])
+    h = 1e-6
+    for causal in (False, True):
+        got = oracle.attn_bwd_dq_rows(q, k, v, do, causal, 0.7, rows, lib=lib)
+
+        def loss(qq):
+            o, _ = oracle.attn_fwd(qq, k, v, causal, 0.7)
+            return float(np.sum(do * o))
+        for r, flat in enumerate(rows):
+            bh, i = divmod(int(flat), 7)
+            for c in range(3):
+                qp, qm = q.copy(), q.copy()
+                qp[0, bh, i, c] += h
+                qm[0, bh, i, c] -= h
+                fd = (loss(qp) - loss(qm)) / (2 * h)
+                assert abs(got[r, c] - fd) <= 1e-7, (causal, flat, c, got[r, c], fd)
+
+
+ALL_CHECKS = [check_dq_rows_finite_differences, check_two_key_golden, check_finite_differences, check_constant_v, check_single_key,
               check_q_zero_closed_form, check_dk_sums_to_zero, check_key_shift_invariance,
               check_linear_in_dout, check_torch_autograd]

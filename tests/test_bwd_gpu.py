@@ -223,3 +223,51 @@ def test_bwd_parity_long_sequence(causal, d):
     got = run_gpu_bwd(q, k, v, do, causal)
     ref = oracle.attn_bwd(q, k, v, do, causal, 1.0 / math.sqrt(d))
     assert_grads_close(got, ref, f"[1,2,8192,{d}] causal={causal}")
+
+
+def _check_sampled(q, k, v, do, got, causal, rows, what):
+    """dQ on sampled rows against the oracle, and the identities that hold at
+    any size: sum_j dV_j = sum_i dO_i (rows of P sum to one) and
+    sum_j dK_j = 0 (rows of dS sum to zero), per head and column."""
+    B, H, N, d = q.shape
+    dq, dk, dv = got
+    ref_dq = oracle.attn_bwd_dq_rows(q, k, v, do, causal, 1.0 / math.sqrt(d), rows)
+    assert_grads_close([dq.reshape(-1, d)[rows]], [ref_dq], f"{what} sampled rows")
+    do64 = do.double().numpy().reshape(B * H, N, d)
+    dv64 = dv.astype(np.float64).reshape(B * H, N, d)
+    dk64 = dk.astype(np.float64).reshape(B * H, N, d)
+    assert np.all(np.abs(dv64.sum(1) - do64.sum(1)) <= 1e-3 * np.abs(dv64).sum(1) + 1e-3), what
+    assert np.all(np.abs(dk64.sum(1)) <= 1e-3 * np.abs(dk64).sum(1) + 1e-6), what
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_bwd_maximum_sequence_length_sampled(causal, d):
+    """N = FA_MAX_N (2^20), one head: 8192 key blocks, each walking up to
+    8192 query blocks (the dQ accumulators take up to 8192 additions per
+    element); sampled dQ rows against the oracle, the dK and dV sums at full
+    size."""
+    N = fa().FA_MAX_N
+    q, k, v, do = grad_inputs(1, 1, N, d, torch.bfloat16, seed=7200 + d)
+    got = run_gpu_bwd(q, k, v, do, causal)
+    rows = sample_rows_bwd(1, 1, N, n_random=6, seed=73)
+    _check_sampled(q, k, v, do, got, causal, rows, f"N=2^20 d={d} causal={causal}")
+
+
+def test_bwd_long_causal_workload_sampled():
+    """The long causal workload [1,32,16384,128] (the forward's default bench
+    shape): sampled dQ rows of eight spread heads, the sums at full size."""
+    from attn_inputs import WORKLOADS, make_workload_inputs
+    w = WORKLOADS["b1h32n16384d128_causal"]
+    q, k, v = make_workload_inputs(w)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(74)
+    do = torch.randn(q.shape, generator=g).to(q.dtype)
+    got = run_gpu_bwd(q, k, v, do, True)
+    rows = sample_rows_bwd(1, 32, w.N, n_random=3, seed=75, heads=range(0, 32, 4))
+    _check_sampled(q, k, v, do, got, True, rows, w.name)
+
+
+def sample_rows_bwd(B, H, N, n_random, seed, heads=None):
+    from attn_inputs import sample_rows
+    return sample_rows(B, H, N, n_random=n_random, seed=seed, heads=heads)

@@ -28,6 +28,21 @@ def test_thread_count_does_not_change_the_result():
             assert np.array_equal(x, y)
 
 
+def test_dq_rows_match_the_full_backward():
+    """The row-sampled dQ equals the full backward oracle's dQ on the same
+    rows (both masks, rows in any order, repeated rows), and rejects rows
+    out of range."""
+    q, k, v = pins.rand_qkv(2, 3, 19, 5, 53, k_mult=2.0)
+    do = np.random.default_rng(54).standard_normal(q.shape)
+    rows = np.array([0, 18, 19, 57, 113, 5, 5, 2 * 3 * 19 - 1])
+    for causal in (False, True):
+        dq, _, _ = oracle.attn_bwd(q, k, v, do, causal, 0.45)
+        got = oracle.attn_bwd_dq_rows(q, k, v, do, causal, 0.45, rows, nthreads=3)
+        assert np.max(np.abs(got - dq.reshape(-1, 5)[rows])) <= 1e-12
+    with pytest.raises(RuntimeError):
+        oracle.attn_bwd_dq_rows(q, k, v, do, False, 0.45, [2 * 3 * 19])
+
+
 def test_bad_arguments():
     q, k, v = pins.rand_qkv(1, 1, 4, 2, 52)
     with pytest.raises(ValueError):
@@ -47,6 +62,10 @@ MUTANTS = [
     ("p_not_normalised", "p[j] = exp(s[j] - m) / l;", "p[j] = exp(s[j] - m);"),
     ("softmax_scale_dropped", "s[j] = jb->scale * dot;", "s[j] = dot;"),
     ("dv_not_reset", "memset(dV, 0, sizeof(double) * (size_t)(N * d));", ""),
+    ("rows_r_dropped", "const double ds = exp(s[j] - m) / l * (dp[j] - rr);",
+     "const double ds = exp(s[j] - m) / l * dp[j];"),
+    ("rows_scale_dropped", "out[c] += jb->scale * ds * K[j * d + c];",
+     "out[c] += ds * K[j * d + c];"),
 ]
 
 
