@@ -228,7 +228,14 @@ def test_bwd_parity_long_sequence(causal, d):
 def _check_sampled(q, k, v, do, got, causal, rows, what):
     """dQ on sampled rows against the oracle, and the identities that hold at
     any size: sum_j dV_j = sum_i dO_i (rows of P sum to one) and
-    sum_j dK_j = 0 (rows of dS sum to zero), per head and column."""
+    sum_j dK_j = 0 (rows of dS sum to zero), per head and column.
+
+    dV and dK accumulate in tensor memory over every query block, 8 MMA
+    steps each, and the tensor core's fp32 accumulation does not round to
+    nearest: the sums drift low by up to 2^-23 per step, coherently across
+    keys (measured: 1.2e-3 at N = 2^20, 65536 steps; 3e-5 at N = 2^14).  The
+    bound on the dV identity is that drift plus 1e-3 for the 16-bit
+    roundings; dK's sum cancels and keeps the plain 1e-3."""
     B, H, N, d = q.shape
     dq, dk, dv = got
     ref_dq = oracle.attn_bwd_dq_rows(q, k, v, do, causal, 1.0 / math.sqrt(d), rows)
@@ -236,8 +243,14 @@ def _check_sampled(q, k, v, do, got, causal, rows, what):
     do64 = do.double().numpy().reshape(B * H, N, d)
     dv64 = dv.astype(np.float64).reshape(B * H, N, d)
     dk64 = dk.astype(np.float64).reshape(B * H, N, d)
-    assert np.all(np.abs(dv64.sum(1) - do64.sum(1)) <= 1e-3 * np.abs(dv64).sum(1) + 1e-3), what
-    assert np.all(np.abs(dk64.sum(1)) <= 1e-3 * np.abs(dk64).sum(1) + 1e-6), what
+    steps = (N + 127) // 128 * 8
+    tol_v = steps * 2.0 ** -23 + 1e-3
+    err_v = np.abs(dv64.sum(1) - do64.sum(1)) / (np.abs(dv64).sum(1) + 1e-3)
+    err_k = np.abs(dk64.sum(1)) / (np.abs(dk64).sum(1) + 1e-6)
+    record("bwd", f"{what} dV-sum identity", rel=err_v.max(), bound=tol_v)
+    record("bwd", f"{what} dK-sum identity", rel=err_k.max(), bound=1e-3)
+    assert err_v.max() <= tol_v, (what, err_v.max(), tol_v)
+    assert err_k.max() <= 1e-3, (what, err_k.max())
 
 
 @pytest.mark.parametrize("d", [64, 128])
