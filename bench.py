@@ -32,8 +32,8 @@ timed region (the library overlaps the copies of one chunk of heads with
 the forward of another).
 
 `--variant` times one of the library's kernel variants (fa_fwd_variant:
-K/V ring depth, share of exponentials on the FMA pipes) instead of the
-default.  `--sweep` times every variant built for the workload's head dim
+K/V ring depth, share of exponentials on the FMA pipes; with --pass bwd,
+fa_bwd_variant's cta_pairs) instead of the default.  `--sweep` times every variant built for the workload's head dim
 and dtype, R rounds in alternating order, and prints a Markdown table of
 median TFLOPS, median SM clock and FLOP per SM clock (the clock-normalised
 rate, which removes the power limit's effect on the clock).
@@ -426,12 +426,15 @@ def run_ours(args, w):
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     call = fa.fa_fwd if w.dtype == "bf16" else fa.fa_fwd_fp16
     variant = parse_variant(args.variant)
-    if variant:
+    bwd = args.pass_ == "bwd"
+    if variant and ("cta_pairs" in variant) != bwd:
+        raise ValueError("cta_pairs is the backward's variant key (with --pass bwd), "
+                         "stages/exp_split/causal_order the forward's")
+    if variant and not bwd:
         def call(q, k, v, o, lse, causal, stream):  # noqa: F811
             fa.fa_fwd_variant(q, k, v, o, lse, causal=causal, stream=stream, **variant)
     stream = torch.cuda.current_stream(dev)
     flops = w.flops()
-    bwd = args.pass_ == "bwd"
     if bwd:
         # the forward once (untimed) for O and LSE; each step is fa_bwd
         o_f, lse_f = fa.forward(q, k, v, causal=w.causal, stream=stream)
@@ -442,7 +445,8 @@ def run_ours(args, w):
                          device=dev)
 
         def call(q, k, v, o, lse, causal, stream):  # noqa: F811
-            fa.fa_bwd(q, k, v, o_f, lse_f, do, dq, dk, dv, ws, causal=causal, stream=stream)
+            fa.fa_bwd(q, k, v, o_f, lse_f, do, dq, dk, dv, ws, causal=causal, stream=stream,
+                      cta_pairs=variant.get("cta_pairs"))
         flops = 2.5 * w.flops()
 
     w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -611,8 +615,9 @@ def parse_variant(text):
             continue
         key, _, val = part.partition("=")
         key = key.strip()
-        if key not in ("stages", "exp_split", "causal_order"):
-            raise ValueError(f"unknown variant key {key!r} (stages, exp_split, causal_order)")
+        if key not in ("stages", "exp_split", "causal_order", "cta_pairs"):
+            raise ValueError(f"unknown variant key {key!r} "
+                             "(stages, exp_split, causal_order; cta_pairs with --pass bwd)")
         out[key] = int(val)
     return out
 
@@ -732,7 +737,8 @@ def main(argv=None):
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="time the forward (default) or the backward")
     ap.add_argument("--variant", default="",
-                    help="kernel variant, e.g. stages=3,exp_split=4 (fa_fwd_variant)")
+                    help="kernel variant, e.g. stages=3,exp_split=4 (fa_fwd_variant), or "
+                         "cta_pairs=1 with --pass bwd (fa_bwd_variant)")
     ap.add_argument("--sweep", action="store_true", help="time every built variant")
     ap.add_argument("--sweep-reps", type=int, default=5)
     ap.add_argument("--sweep-idle", type=float, default=0.5,

@@ -17,7 +17,7 @@ import math
 import os
 
 __all__ = ["FaError", "fa_fwd_host", "fa_fwd_noalloc", "fa_fwd", "fa_fwd_fp16", "fa_fwd_ex",
-           "fa_fwd_variant", "fa_bwd", "fa_bwd_workspace_size", "fa_get_status", "fa_strerror",
+           "fa_fwd_variant", "fa_bwd", "fa_bwd_variant", "fa_bwd_workspace_size", "fa_get_status", "fa_strerror",
            "fa_version", "forward", "backward", "library_path", "lib", "variants"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -88,6 +88,10 @@ def lib():
         L.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, I64, I64, I64, I64,
                              ctypes.c_int, ctypes.c_float, ctypes.c_int, P]
         L.fa_bwd.restype = ctypes.c_int
+        L.fa_bwd_variant.argtypes = [P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, I64, I64, I64,
+                                     I64, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                     P]
+        L.fa_bwd_variant.restype = ctypes.c_int
         L.fa_bwd_workspace_size.argtypes = [I64, I64, I64, I64, ctypes.POINTER(ctypes.c_size_t)]
         L.fa_bwd_workspace_size.restype = ctypes.c_int
         L.fa_variant_count.argtypes = []
@@ -235,11 +239,14 @@ def fa_bwd_workspace_size(B, H, N, d) -> int:
 
 
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, causal=False, scale=None,
-           stream=None) -> None:
+           stream=None, cta_pairs=None) -> None:
     """Attention backward into caller-provided dq, dk, dv [B,H,N,d] (dtype of
     q) from the forward's q, k, v, o, lse and the output gradient dout;
     `workspace` is a CUDA uint8 tensor of at least fa_bwd_workspace_size
-    bytes (256-byte aligned, as torch allocates)."""
+    bytes (256-byte aligned, as torch allocates).  cta_pairs = None calls
+    fa_bwd (the library's default kernel); 0 or 1 calls fa_bwd_variant with
+    that kernel: one CTA per key block, or clusters of two CTAs that halve
+    the dQ additions."""
     import torch
     if q.dim() != 4:
         raise ValueError("q must be [B, H, N, d]")
@@ -254,22 +261,25 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, causal=False, scale=Non
         raise ValueError("workspace must be a contiguous CUDA tensor")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    rc = lib().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                      dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                      workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                      B, H, N, d, int(bool(causal)), float(scale), int(q.dtype == torch.float16),
-                      _stream_handle(stream, q.device))
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+            dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+            B, H, N, d, int(bool(causal)), float(scale), int(q.dtype == torch.float16))
+    if cta_pairs is None:
+        rc = lib().fa_bwd(*args, _stream_handle(stream, q.device))
+    else:
+        rc = lib().fa_bwd_variant(*args, int(cta_pairs), _stream_handle(stream, q.device))
     if rc != FA_OK:
-        raise FaError(rc, "fa_bwd")
+        raise FaError(rc, "fa_bwd" if cta_pairs is None else "fa_bwd_variant")
 
 
-def backward(q, k, v, o, lse, dout, causal=False, scale=None, stream=None):
+def backward(q, k, v, o, lse, dout, causal=False, scale=None, stream=None, cta_pairs=None):
     """Allocate dq, dk, dv and the workspace with torch and run the backward;
     returns (dq, dk, dv)."""
     import torch
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(fa_bwd_workspace_size(*q.shape), dtype=torch.uint8, device=q.device)
-    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, ws, causal, scale, stream)
+    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, ws, causal, scale, stream, cta_pairs)
     return dq, dk, dv
 
 

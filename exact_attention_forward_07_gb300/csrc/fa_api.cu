@@ -61,8 +61,8 @@ struct DeviceState {
   size_t stage_bytes = 0;
   std::once_flag attr_once[kMaxVariants];  // shared-memory attribute, per kernel variant
   int attr_err[kMaxVariants] = {};
-  std::once_flag bwd_attr_once[4];  // backward kernels: [d == 128][fp16]
-  int bwd_attr_err[4] = {};
+  std::once_flag bwd_attr_once[8];  // backward kernels: [d == 128][fp16][CTA pairs]
+  int bwd_attr_err[8] = {};
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -557,13 +557,17 @@ int bwd_shape_check(int64_t B, int64_t H, int64_t N, int64_t d) {
   return FA_OK;
 }
 
-template <int D, bool BF16>
+// fa_bwd's kernel: one CTA per key block (false) or clusters of two that
+// halve the dQ additions (true); fa_bwd_variant reaches both.
+constexpr bool kBwdPairDefault = false;
+
+template <int D, bool BF16, bool PAIR>
 int launch_bwd(DeviceState &ds, const void *q, const void *k, const void *v, const void *o,
                const float *lse, const void *dout, void *dq, void *dk, void *dv,
                uint8_t *ws, int64_t BH, int64_t N, int causal, float scale, cudaStream_t stream) {
   using C = fa::BwdCfg<D, BF16>;
-  auto kernel = fa::fa_bwd_kernel<D, BF16>;
-  const int slot = (D == 128 ? 2 : 0) + (BF16 ? 0 : 1);
+  auto kernel = fa::fa_bwd_kernel<D, BF16, PAIR>;
+  const int slot = (D == 128 ? 4 : 0) + (BF16 ? 0 : 2) + (PAIR ? 1 : 0);
   std::call_once(ds.bwd_attr_once[slot], [&] {
     ds.bwd_attr_err[slot] = static_cast<int>(
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
@@ -596,16 +600,82 @@ int launch_bwd(DeviceState &ds, const void *q, const void *k, const void *v, con
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   const dim3 tiles(static_cast<unsigned>(p.n_tiles), static_cast<unsigned>(BH));
   fa::fa_bwd_prep_kernel<D, BF16><<<tiles, 256, 0, stream>>>(p);
-  kernel<<<static_cast<unsigned>(BH * p.n_tiles), C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv,
-                                                                                         tdo, p);
-  fa::fa_bwd_dq_kernel<D, BF16><<<tiles, 128, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  if constexpr (PAIR) {
+    // clusters of two CTAs over adjacent key blocks; an odd count of key
+    // blocks per head gets one idle CTA to complete its last cluster
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(BH * (p.n_tiles + (p.n_tiles & 1))));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, tdo, p);
+  } else {
+    kernel<<<static_cast<unsigned>(BH * p.n_tiles), C::kThreads, C::kSmemBytes, stream>>>(
+        tq, tk, tv, tdo, p);
+  }
+  if (e == cudaSuccess) fa::fa_bwd_dq_kernel<D, BF16><<<tiles, 128, 0, stream>>>(p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
       return FA_ERR_DEVICE;
     return cuda_fail(e);
   }
   return FA_OK;
+}
+
+int bwd_common(const void *q, const void *k, const void *v, const void *o, const float *lse,
+               const void *dout, void *dq, void *dk, void *dv, void *workspace,
+               size_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t d, int causal,
+               float scale, int fp16, bool pair, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace)
+    return FA_ERR_NULL;
+  int rc = bwd_shape_check(B, H, N, d);
+  if (rc != FA_OK) return rc;
+  if (B * H > 65535) return FA_ERR_SHAPE;  // grid y of the row kernels
+  for (const void *ptr : {q, k, v, o, dout, static_cast<const void *>(dq),
+                          static_cast<const void *>(dk), static_cast<const void *>(dv)})
+    if (reinterpret_cast<uintptr_t>(ptr) & 15u) return FA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGN;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+  const int64_t BH = B * H;
+  const BwdWorkspace w = bwd_workspace(BH, N, d);
+  if (workspace_bytes < w.total) return FA_ERR_WORKSPACE;
+  const size_t tb = static_cast<size_t>(BH * N * d) * 2, lb = static_cast<size_t>(BH * N) * 4;
+  const void *outs[3] = {dq, dk, dv};
+  for (int a = 0; a < 3; ++a) {
+    for (const void *in : {q, k, v, o, dout})
+      if (overlaps(outs[a], tb, in, tb)) return FA_ERR_ALIAS;
+    if (overlaps(outs[a], tb, lse, lb) || overlaps(outs[a], tb, workspace, w.total))
+      return FA_ERR_ALIAS;
+    for (int b = a + 1; b < 3; ++b)
+      if (overlaps(outs[a], tb, outs[b], tb)) return FA_ERR_ALIAS;
+  }
+  for (const void *in : {q, k, v, o, dout})
+    if (overlaps(workspace, w.total, in, tb)) return FA_ERR_ALIAS;
+  if (overlaps(workspace, w.total, lse, lb)) return FA_ERR_ALIAS;
+
+  DeviceState *ds = nullptr;
+  rc = device_state(&ds);
+  if (rc != FA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+#define FA_BWD(DD, BB, PP) launch_bwd<DD, BB, PP>(*ds, q, k, v, o, lse, dout, dq, dk, dv, ws, BH, N, causal, scale, st)
+  if (pair) {
+    if (d == 64) return fp16 ? FA_BWD(64, false, true) : FA_BWD(64, true, true);
+    return fp16 ? FA_BWD(128, false, true) : FA_BWD(128, true, true);
+  }
+  if (d == 64) return fp16 ? FA_BWD(64, false, false) : FA_BWD(64, true, false);
+  return fp16 ? FA_BWD(128, false, false) : FA_BWD(128, true, false);
+#undef FA_BWD
 }
 
 }  // namespace
@@ -663,43 +733,17 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            const void *dout, void *dq, void *dk, void *dv, void *workspace,
            size_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t d, int causal,
            float scale, int fp16, fa_stream_t stream) {
-  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace)
-    return FA_ERR_NULL;
-  int rc = bwd_shape_check(B, H, N, d);
-  if (rc != FA_OK) return rc;
-  if (B * H > 65535) return FA_ERR_SHAPE;  // grid y of the row kernels
-  for (const void *ptr : {q, k, v, o, dout, static_cast<const void *>(dq),
-                          static_cast<const void *>(dk), static_cast<const void *>(dv)})
-    if (reinterpret_cast<uintptr_t>(ptr) & 15u) return FA_ERR_ALIGN;
-  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_ALIGN;
-  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGN;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
-  const int64_t BH = B * H;
-  const BwdWorkspace w = bwd_workspace(BH, N, d);
-  if (workspace_bytes < w.total) return FA_ERR_WORKSPACE;
-  const size_t tb = static_cast<size_t>(BH * N * d) * 2, lb = static_cast<size_t>(BH * N) * 4;
-  const void *outs[3] = {dq, dk, dv};
-  for (int a = 0; a < 3; ++a) {
-    for (const void *in : {q, k, v, o, dout})
-      if (overlaps(outs[a], tb, in, tb)) return FA_ERR_ALIAS;
-    if (overlaps(outs[a], tb, lse, lb) || overlaps(outs[a], tb, workspace, w.total))
-      return FA_ERR_ALIAS;
-    for (int b = a + 1; b < 3; ++b)
-      if (overlaps(outs[a], tb, outs[b], tb)) return FA_ERR_ALIAS;
-  }
-  for (const void *in : {q, k, v, o, dout})
-    if (overlaps(workspace, w.total, in, tb)) return FA_ERR_ALIAS;
-  if (overlaps(workspace, w.total, lse, lb)) return FA_ERR_ALIAS;
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H, N, d,
+                    causal, scale, fp16, kBwdPairDefault, stream);
+}
 
-  DeviceState *ds = nullptr;
-  rc = device_state(&ds);
-  if (rc != FA_OK) return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  uint8_t *ws = static_cast<uint8_t *>(workspace);
-#define FA_BWD(DD, BB) launch_bwd<DD, BB>(*ds, q, k, v, o, lse, dout, dq, dk, dv, ws, BH, N, causal, scale, st)
-  if (d == 64) return fp16 ? FA_BWD(64, false) : FA_BWD(64, true);
-  return fp16 ? FA_BWD(128, false) : FA_BWD(128, true);
-#undef FA_BWD
+int fa_bwd_variant(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                   const void *dout, void *dq, void *dk, void *dv, void *workspace,
+                   size_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t d,
+                   int causal, float scale, int fp16, int cta_pairs, fa_stream_t stream) {
+  if (cta_pairs != 0 && cta_pairs != 1) return FA_ERR_OPTION;
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H, N, d,
+                    causal, scale, fp16, cta_pairs == 1, stream);
 }
 
 int fa_variant_count(void) { return kNumVariants; }

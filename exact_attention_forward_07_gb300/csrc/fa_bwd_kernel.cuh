@@ -23,6 +23,11 @@
 //                        TMA ring of Q_i and dO_i; five tcgen05 MMAs per step
 //   fa_bwd_dq_kernel     dQ = scale * accumulators, rounded to 16 bits
 //
+// fa_bwd_kernel<PAIR = true> runs the same CTAs in clusters of two over
+// adjacent key blocks, which exchange halves of each dQ product through
+// distributed shared memory and so add half as many bytes to the fp32
+// accumulators (the additions, not the MMAs, bound the one-CTA kernel).
+//
 // Roles in fa_bwd_kernel (640 threads):
 //   warp  0     TMA producer (one thread)
 //   warp  1     MMA issue (one elected lane) + tensor-memory allocation
@@ -88,9 +93,13 @@ struct BwdCfg {
   static constexpr int kBar = kDd + 2 * 512;
   // barriers: K/V loaded; Q/dO stage full (2) and empty (2); S^T and dP^T
   // done; dS written and dQ read (one arrival per compute warp each); dQ
-  // done; dK/dV done; drain
+  // done; dK/dV done; drain; and for CTA pairs: the peer may write into
+  // this CTA's dS buffer (arrived by the peer), the peer's dQ columns have
+  // landed there (one local arrival + the bytes)
   static constexpr int bKV = 0, bFull = 1, bEmpty = 3, bSdp = 5, bDs = 6, bDqFull = 7,
-                       bDqFree = 8, bDkdv = 9, bDrain = 10, kNumBars = 11;
+                       bDqFree = 8, bDkdv = 9, bDrain = 10, bSendOk = 11, bRecv = 12,
+                       kNumBars = 13;
+  static constexpr uint32_t kRecvBytes = 128 * (D / 2) * 4;  // half of dQ's columns, fp32
   static constexpr int kMisc = kBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kUsed = kMisc + 16;
   // 1 KiB of slack for the 1024-byte alignment of the tiles when it fits in
@@ -189,7 +198,35 @@ __global__ void __launch_bounds__(128) fa_bwd_dq_kernel(const BwdParams p) {
   }
 }
 
-template <int D, bool BF16>
+// Bounded wait on a barrier that the other CTA of the pair arrives on or
+// writes through (acquire at cluster scope); false = give up.
+__device__ __forceinline__ bool wait_bar_cl(uint32_t bar, uint32_t parity,
+                                            volatile int *abort_flag, unsigned *status) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        atomicOr(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// PAIR: CTAs run in clusters of two over adjacent key blocks 2c and 2c + 1
+// of one head.  Both visit the same query blocks (causal: the even block's
+// first, its diagonal, alone), and for each such block the pair halves its
+// dQ additions: dQ_i = dS_i,2c K_2c + dS_i,2c+1 K_2c+1, so each CTA sends
+// the peer the 16-column groups of its dQ product that the peer adds to
+// L2 (st.async into the peer's dS buffer, free once the peer's dK and dQ
+// MMAs have read it) and adds the peer's groups to its own before its
+// reductions.  The pages' backward notes reach the same saving with two
+// CTAs sharing one larger MMA tile.
+template <int D, bool BF16, bool PAIR>
 __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -212,12 +249,20 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31u;
   // this CTA's key block; the CTAs of one head are consecutive, heaviest
-  // (causal: the first key block sees every query block) first
+  // (causal: the first key block sees every query block) first.  PAIR: an
+  // odd count of key blocks is completed by an idle CTA, so that clusters
+  // of two never straddle heads; the block before it works alone.
   const int T = p.n_tiles;
-  const int bh = blockIdx.x / T;
-  const int jb = blockIdx.x - bh * T;
+  const int Tg = PAIR ? T + (T & 1) : T;
+  const int bh = blockIdx.x / Tg;
+  const int jb = blockIdx.x - bh * Tg;
+  const bool idle = PAIR && jb >= T;
+  const uint32_t rank = PAIR ? static_cast<uint32_t>(jb & 1) : 0u;  // rank in the cluster
+  const bool paired = PAIR && !idle && (jb ^ 1) < T;
   const int i0 = p.causal ? jb : 0;
-  const int n_steps = T - i0;
+  const int n_steps = idle ? 0 : T - i0;
+  // first step whose query block the peer visits too
+  const int xs0 = (p.causal && rank == 0) ? 1 : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::bKV), 1);
@@ -231,6 +276,8 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     mbar_init(bar(C::bDqFree), C::kComputeWarps);  // one arrival per compute warp
     mbar_init(bar(C::bDkdv), 1);
     mbar_init(bar(C::bDrain), 1);
+    mbar_init(bar(C::bSendOk), 1);  // the peer's one arrival per shared query block
+    mbar_init(bar(C::bRecv), 1);    // this CTA's expect-bytes arrival
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -248,10 +295,12 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_base_slot;
+  // the peer's barriers are initialised before either CTA signals the other
+  if constexpr (PAIR) cluster_sync();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (lane == 0 && !idle) {
       const uint64_t pol_once = l2_policy_evict_first();  // K_j, V_j: read by this CTA only
       const uint64_t pol_reuse = l2_policy_evict_last();  // Q_i, dO_i: read by every CTA of the head
       mbar_arrive_expect_tx(bar(C::bKV), 2 * C::kTile);
@@ -283,7 +332,7 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
         if (cnt > 0) wait_drain(bar(C::bFull + s), (cnt - 1) & 1u, abort_flag, p.status);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 && !idle) {
     // ------------------------------------------------------------- MMA issue
     const uint32_t leader = elect_one();
     const uint64_t kdesc0 = smem_desc_sw128(0, 16, 1024);       // K-major tiles
@@ -292,7 +341,7 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     // of 64-column halves (the layout TMA writes)
     auto ss_kk = [&](uint32_t dcol, uint32_t a, uint32_t b, uint32_t idesc, int ksteps,
                      bool acc) {
-      const uint64_t ad = kdesc0 + (a >> 4), bd = kdesc0 + (b >> 4);
+      const uint64_t ad = kdesc0 + desc_addr(a), bd = kdesc0 + desc_addr(b);
       for (int kk = 0; kk < ksteps; ++kk) {
         const uint32_t off = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;
         mma_ss_if(leader, tmem + dcol, ad + off, bd + off, idesc, (acc || kk > 0) ? 1u : 0u);
@@ -315,12 +364,12 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       tc_fence_after();
       // dV += P^T dO: P^T packed in tensor memory, query slice c (32
       // queries) at columns [32c, 32c + 16)
-      const uint64_t bdo = mdesc0 + (do_s >> 4), bq = mdesc0 + (q_s >> 4);
+      const uint64_t bdo = mdesc0 + desc_addr(do_s), bq = mdesc0 + desc_addr(q_s);
       for (int kk = 0; kk < 8; ++kk)
         mma_ts_if(leader, tmem + C::cDV, tmem + C::cS + 32 * (kk >> 1) + 8 * (kk & 1),
                   bdo + kk * (2048 >> 4), C::kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
       // dK += dS^T Q: dS^T K-major in shared memory, Q MN-major
-      const uint64_t ads = kdesc0 + ((sbase + C::kDS) >> 4);
+      const uint64_t ads = kdesc0 + desc_addr(sbase + C::kDS);
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;
         mma_ss_if(leader, tmem + C::cDK, ads + off, bq + kk * (2048 >> 4), C::kIdescG,
@@ -331,7 +380,7 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
         tc_fence_after();
       }
       // dQ = dS K: the same buffer read MN-major, K MN-major
-      const uint64_t adt = mdesc0 + ((sbase + C::kDS) >> 4), bk = mdesc0 + ((sbase + C::kK) >> 4);
+      const uint64_t adt = mdesc0 + desc_addr(sbase + C::kDS), bk = mdesc0 + desc_addr(sbase + C::kK);
       for (int kk = 0; kk < 8; ++kk)
         mma_ss_if(leader, tmem + C::cDQ, adt + kk * (2048 >> 4), bk + kk * (2048 >> 4), C::kIdescQ,
                   kk > 0 ? 1u : 0u);
@@ -341,7 +390,7 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     if (ok) mma_commit_if(leader, bar(C::bDkdv));
     mma_commit_if(leader, bar(C::bDrain));
     wait_drain(bar(C::bDrain), 0, abort_flag, p.status);
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && !idle) {
     // --------------------------------------------------------- compute warps
     // Sixteen warps; warp w owns the keys of lane quadrant w % 4 (one thread
     // per key) and the 32 query columns [32 cs, 32 cs + 32) of S^T, dP^T,
@@ -357,9 +406,17 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     const uint64_t sl2_2 = f2(p.scale_log2, p.scale_log2);
     // this key's 128-byte row of dS^T in half cs / 2 of the query columns
     uint8_t *ds_row = smem + C::kDS + (cs >> 1) * C::kHalf + row * 128;
+    // PAIR: the peer's dS buffer and barriers, as seen from this CTA
+    const uint32_t peer_buf = PAIR ? mapa_shared(sbase + C::kDS, rank ^ 1u) : 0u;
+    const uint32_t peer_send_ok = PAIR ? mapa_shared(bar(C::bSendOk), rank ^ 1u) : 0u;
+    const uint32_t peer_recv = PAIR ? mapa_shared(bar(C::bRecv), rank ^ 1u) : 0u;
     bool ok = true;
     for (int t = 0; ok && t < n_steps; ++t) {
-      if (!(ok = wait_bar(bar(C::bSdp), t & 1u, abort_flag, p.status))) break;
+      // query block shared with the peer: every warp takes the same branch
+      const bool xchg = paired && t >= xs0;
+      const uint32_t xpar = static_cast<uint32_t>(t - xs0) & 1u;
+      ok = wait_bar(bar(C::bSdp), t & 1u, abort_flag, p.status);
+      if (ok) {
       tc_fence_after();
       const int s = t & 1, i = i0 + t;
       const float *lse2s = reinterpret_cast<const float *>(smem + C::kLse + s * 512);
@@ -413,11 +470,20 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::bDs));
+      }
       // phase 2: dQ of this step (query rows of this quadrant, 32 columns)
       // into registers; its tensor-memory columns are released before the
       // additions are issued, so the next step's MMAs overlap them
-      if (!(ok = wait_bar(bar(C::bDqFull), t & 1u, abort_flag, p.status))) break;
+      if (ok) ok = wait_bar(bar(C::bDqFull), t & 1u, abort_flag, p.status);
+      if (ok) {
       tc_fence_after();
+      const int i = i0 + t;
+      if (PAIR && xchg && w == 0 && lane == 0) {
+        // this CTA's dK and dQ MMAs have read its dS buffer: the peer may
+        // write its columns there
+        mbar_arrive_expect_tx(bar(C::bRecv), C::kRecvBytes);
+        mbar_arrive_remote(peer_send_ok);
+      }
       uint32_t r[32];
       if (32 * cs < D) {
         tmem_ld32(t_lane + C::cDQ + 32 * cs, r);
@@ -429,11 +495,49 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       if (32 * cs < D) {
         float4 *dst = p.dq_acc + (static_cast<size_t>(bh) * T + i) * (D / 4) * 128 + row +
                       8 * cs * 128;
+        if (PAIR && xchg) {
+          // columns 32 cs + 16 k + [0, 16) belong to rank k: send the
+          // peer's sixteen, then add the peer's to this CTA's own
+          uint32_t mine[16], theirs[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          red_add_v4(dst + u * 128, __uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
-                     __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+          for (int e = 0; e < 16; ++e) {
+            mine[e] = rank ? r[16 + e] : r[e];
+            theirs[e] = rank ? r[e] : r[16 + e];
+          }
+          ok = wait_bar_cl(bar(C::bSendOk), xpar, abort_flag, p.status);
+          if (ok) {
+#pragma unroll
+            for (uint32_t u = 0; u < 4; ++u)
+              st_async_v4(peer_buf + ((((4u * cs + u) << 7) + static_cast<uint32_t>(row)) << 4),
+                          theirs[4 * u], theirs[4 * u + 1], theirs[4 * u + 2], theirs[4 * u + 3],
+                          peer_recv);
+            ok = wait_bar_cl(bar(C::bRecv), xpar, abort_flag, p.status);
+          }
+          if (ok) {
+            const float4 *in = reinterpret_cast<const float4 *>(smem + C::kDS) + 4 * cs * 128 + row;
+            float4 *dm = dst + 4 * rank * 128;
+#pragma unroll
+            for (uint32_t u = 0; u < 4; ++u) {
+              const float4 x = in[u * 128];
+              red_add_v4(dm + u * 128, __uint_as_float(mine[4 * u]) + x.x,
+                         __uint_as_float(mine[4 * u + 1]) + x.y,
+                         __uint_as_float(mine[4 * u + 2]) + x.z,
+                         __uint_as_float(mine[4 * u + 3]) + x.w);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            red_add_v4(dst + u * 128, __uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                       __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+        }
       }
+      }
+      // PAIR: no compute warp writes the next dS before all have read the
+      // peer's columns out of the same buffer; taken on every step of a
+      // paired CTA, so that a warp whose wait gave up leaves the loop at the
+      // same step as all the others
+      if (PAIR && paired) ok = bar_and(1, 32 * C::kComputeWarps, ok);
     }
     // epilogue: dK (times scale) and dV of this quadrant's keys; 32 columns
     // each: d = 128, slice cs of both; d = 64, slices 0-1 take dK and 2-3 dV
@@ -472,6 +576,8 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
   }
 
   __syncthreads();
+  // neither CTA of a pair leaves while the other may still signal it
+  if constexpr (PAIR) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);

@@ -316,6 +316,16 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
          (2ull << 61);
 }
 
+// The start-address field of a matrix descriptor for shared address
+// `saddr`: bits 4-17.  A CTA launched in a cluster sees shared addresses
+// with bits set above bit 17 (measured: unmasked, they carried into the
+// leading-byte-offset field and broke every MN-major operand that spans
+// two swizzle atoms), so the address is masked before it is added to a
+// descriptor.
+__device__ __forceinline__ uint64_t desc_addr(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and
 // B element type (bits 7-9, 10-12: 0 = f16, 1 = bf16), operand majorness
 // (bit 15 A, bit 16 B: 0 = K-major, 1 = MN-major), N >> 3 (bits 17-22),
@@ -350,6 +360,78 @@ __device__ __forceinline__ void red_add_v4(float4 *addr, float a, float b, float
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
                "f"(c), "f"(d)
                : "memory");
+}
+
+// ------------------------------------------------------ thread-block clusters
+// Rank of this CTA in its cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The shared-memory address at the same offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive on a barrier of another CTA of the cluster (an address from
+// mapa_shared), releasing this thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+
+// try_wait acquiring at cluster scope: for barriers that other CTAs of the
+// cluster arrive on or write through.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// 16 bytes into another CTA's shared memory (16-byte aligned address from
+// mapa_shared); the write counts 16 bytes on that CTA's barrier
+// `cluster_bar` when it lands.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
+                                            uint32_t c, uint32_t d, uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(cluster_addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
+      : "memory");
+}
+
+// Every thread of every CTA of the cluster arrives, then waits for all.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
+// Named barrier `id` over `nthreads` threads (whole warps) that returns the
+// AND of every participant's `pred` (the form that allows a warp's threads
+// to arrive apart).
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // ------------------------------------------------------------ arithmetic

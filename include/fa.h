@@ -264,6 +264,20 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            size_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t d, int causal,
            float scale, int fp16, fa_stream_t stream);
 
+/* fa_bwd_variant -- fa_bwd with its kernel chosen: cta_pairs = 0 runs one
+ * CTA per 128-key block, each adding its dQ products into the fp32
+ * workspace; cta_pairs = 1 runs clusters of two CTAs over adjacent key
+ * blocks that exchange halves of their dQ products through distributed
+ * shared memory, so that each query block's dQ gets half as many additions
+ * (the saving the pages' backward notes obtain with two CTAs sharing one
+ * larger MMA tile).  Same arguments, results and errors as fa_bwd (within
+ * rounding: the additions are grouped differently), plus FA_ERR_OPTION for
+ * another cta_pairs value. */
+int fa_bwd_variant(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                   const void *dout, void *dq, void *dk, void *dv, void *workspace,
+                   size_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t d,
+                   int causal, float scale, int fp16, int cta_pairs, fa_stream_t stream);
+
 /* fa_bwd_workspace_size -- bytes of workspace fa_bwd needs for [B,H,N,d]:
  * B*H*Np*(4*d + 8) with Np = N rounded up to a multiple of 128.  Host only.
  * FA_ERR_NULL / FA_ERR_SHAPE / FA_ERR_HEADDIM / FA_ERR_UNSUPPORTED_N. */

@@ -215,6 +215,22 @@ def test_fa_bwd_argument_errors(lib):
     assert bwd(ws=DO) == fa.FA_ERR_ALIAS
     assert bwd(dk=WS + 4096) == fa.FA_ERR_ALIAS
     assert bwd(lse=DV + 64) == fa.FA_ERR_ALIAS
+    # fa_bwd_variant: the same checks, and only cta_pairs 0 or 1
+
+    def bwdv(pairs, **kw):
+        a = dict(q=Q, k=K, v=V, o=O, lse=L, do=DO, dq=DQ, dk=DK, dv=DV, ws=WS, B=2, H=3,
+                 N=1000, d=128, causal=0, scale=0.125, fp16=0)
+        a.update(kw)
+        return lib.fa_bwd_variant(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"],
+                                  a["dk"], a["dv"], a["ws"], need, a["B"], a["H"], a["N"], a["d"],
+                                  a["causal"], a["scale"], a["fp16"], pairs, None)
+    for bad in (-1, 2, 7):
+        assert bwdv(bad) == fa.FA_ERR_OPTION
+    for pairs in (0, 1):
+        assert bwdv(pairs, do=None) == fa.FA_ERR_NULL
+        assert bwdv(pairs, d=96) == fa.FA_ERR_HEADDIM
+        assert bwdv(pairs, dq=DQ + 8) == fa.FA_ERR_ALIGN
+        assert bwdv(pairs, dv=DK) == fa.FA_ERR_ALIAS
     n = ctypes.c_size_t()
     assert lib.fa_bwd_workspace_size(1, 1, 128, 64, None) == fa.FA_ERR_NULL
     assert lib.fa_bwd_workspace_size(1, 1, 128, 32, ctypes.byref(n)) == fa.FA_ERR_HEADDIM

@@ -42,11 +42,12 @@ def grad_inputs(B, H, N, d, dtype, seed, k_mult=1.0):
     return q, k, v, do
 
 
-def run_gpu_bwd(q, k, v, do, causal, scale=None):
+def run_gpu_bwd(q, k, v, do, causal, scale=None, cta_pairs=None):
     dev = torch.device("cuda")
     qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
     o, lse = fa().forward(qd, kd, vd, causal=causal, scale=scale)
-    dq, dk, dv = fa().backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    dq, dk, dv = fa().backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale,
+                               cta_pairs=cta_pairs)
     torch.cuda.synchronize()
     assert fa().fa_get_status() == 0
     return [x.float().cpu().numpy() for x in (dq, dk, dv)]
@@ -284,3 +285,49 @@ def test_bwd_long_causal_workload_sampled():
 def sample_rows_bwd(B, H, N, n_random, seed, heads=None):
     from attn_inputs import sample_rows
     return sample_rows(B, H, N, n_random=n_random, seed=seed, heads=heads)
+
+
+# Shapes for the kernel that runs CTAs in clusters of two (fa_bwd_variant,
+# cta_pairs = 1): one key block (a working CTA and an idle one), two (one
+# pair), three (a pair and a lone block), ragged and longer sequences.
+PAIR_SHAPES = [
+    (1, 1, 1, 64, torch.bfloat16),
+    (1, 2, 100, 128, torch.bfloat16),
+    (1, 2, 256, 128, torch.bfloat16),
+    (1, 2, 384, 64, torch.float16),
+    (2, 3, 1000, 128, torch.bfloat16),
+    (1, 2, 2048 + 77, 128, torch.bfloat16),
+    (2, 2, 1024, 64, torch.bfloat16),
+    (1, 1, 4096, 128, torch.float16),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("B,H,N,d,dtype", PAIR_SHAPES,
+                         ids=[f"b{b}h{h}n{n}d{d}-{str(t)[6:]}" for b, h, n, d, t in PAIR_SHAPES])
+def test_bwd_cta_pairs_parity(B, H, N, d, dtype, causal):
+    """The paired kernel against the oracle, and against the one-CTA kernel:
+    dK and dV come from the same MMAs in the same order (bitwise equal);
+    dQ only groups its fp32 additions differently."""
+    q, k, v, do = grad_inputs(B, H, N, d, dtype, seed=1700 + N + d)
+    got = run_gpu_bwd(q, k, v, do, causal, cta_pairs=1)
+    ref = oracle.attn_bwd(q, k, v, do, causal, 1.0 / math.sqrt(d))
+    assert_grads_close(got, ref, f"pairs {B},{H},{N},{d},{dtype},causal={causal}")
+    single = run_gpu_bwd(q, k, v, do, causal, cta_pairs=0)
+    assert np.array_equal(got[1], single[1]) and np.array_equal(got[2], single[2])
+    scale_q = max(np.abs(single[0]).max(), 1e-3)
+    assert np.abs(got[0] - single[0]).max() <= 2.0 ** -7 * scale_q
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_bwd_cta_pairs_bench_shape_heads(causal):
+    """[8,16,4096,128] bf16 through the paired kernel, three heads against
+    the oracle."""
+    B, H, N, d = 8, 16, 4096, 128
+    q, k, v, do = grad_inputs(B, H, N, d, torch.bfloat16, seed=900)
+    got = run_gpu_bwd(q, k, v, do, causal, cta_pairs=1)
+    heads = [0, 61, 127]
+    sub = [x.reshape(B * H, 1, N, d)[heads].reshape(1, len(heads), N, d) for x in (q, k, v, do)]
+    ref = oracle.attn_bwd(*sub, causal, 1.0 / math.sqrt(d))
+    got = [g.reshape(B * H, N, d)[heads].reshape(1, len(heads), N, d) for g in got]
+    assert_grads_close(got, ref, f"pairs [8,16,4096,128] causal={causal}")
