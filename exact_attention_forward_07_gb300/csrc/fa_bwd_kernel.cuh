@@ -198,6 +198,16 @@ __global__ void __launch_bounds__(128) fa_bwd_dq_kernel(const BwdParams p) {
   }
 }
 
+// NG groups of four fp32 additions: v[4u .. 4u + 3] into dst[128 u], the
+// accumulator layout's float4 columns of one row.
+template <int NG>
+__device__ __forceinline__ void red_groups(float4 *dst, const uint32_t *v) {
+#pragma unroll
+  for (int u = 0; u < NG; ++u)
+    red_add_v4(dst + u * 128, __uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+               __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+}
+
 // Bounded wait on a barrier that the other CTA of the pair arrives on or
 // writes through (acquire at cluster scope); false = give up.
 __device__ __forceinline__ bool wait_bar_cl(uint32_t bar, uint32_t parity,
@@ -410,6 +420,16 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     const uint32_t peer_buf = PAIR ? mapa_shared(sbase + C::kDS, rank ^ 1u) : 0u;
     const uint32_t peer_send_ok = PAIR ? mapa_shared(bar(C::bSendOk), rank ^ 1u) : 0u;
     const uint32_t peer_recv = PAIR ? mapa_shared(bar(C::bRecv), rank ^ 1u) : 0u;
+    // d = 128: half of each step's dQ additions are deferred into the next
+    // step's softmax, two float4 groups per sub-chunk.  Issued all at once,
+    // the eight additions per thread fill the load/store queue and hold the
+    // warps past the point where the next S^T and dP^T are ready (the chip
+    // takes fp32 additions at about twice the rate this kernel issues them);
+    // spread out they drain while the exponentials run.  At d = 64 the extra
+    // sixteen registers spill, so it keeps the single burst.
+    constexpr bool kDefer = (D == 128) && !PAIR;
+    uint32_t pend[16];
+    float4 *pend_dst = nullptr;
     bool ok = true;
     for (int t = 0; ok && t < n_steps; ++t) {
       // query block shared with the peer: every warp takes the same branch
@@ -430,6 +450,10 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
         tmem_ld16(t_lane + C::cDP + q0, dr);
         tmem_ld_wait(sr);
         tmem_ld_wait(dr);
+        if constexpr (kDefer) {
+          if (pend_dst != nullptr) red_groups<2>(pend_dst + (4 + 2 * sc) * 128, pend + 8 * sc);
+          if (sc == 1) pend_dst = nullptr;
+        }
         uint32_t pk[8], gk[8];
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
@@ -525,11 +549,13 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
                          __uint_as_float(mine[4 * u + 3]) + x.w);
             }
           }
-        } else {
+        } else if (kDefer) {
+          red_groups<4>(dst, r);
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            red_add_v4(dst + u * 128, __uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
-                       __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+          for (int e = 0; e < 16; ++e) pend[e] = r[16 + e];
+          pend_dst = dst;
+        } else {
+          red_groups<8>(dst, r);
         }
       }
       }
@@ -539,6 +565,7 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       // same step as all the others
       if (PAIR && paired) ok = bar_and(1, 32 * C::kComputeWarps, ok);
     }
+    if (kDefer && pend_dst != nullptr) red_groups<4>(pend_dst + 4 * 128, pend);
     // epilogue: dK (times scale) and dV of this quadrant's keys; 32 columns
     // each: d = 128, slice cs of both; d = 64, slices 0-1 take dK and 2-3 dV
     ok = __all_sync(0xffffffffu, ok);
