@@ -425,10 +425,11 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     // the eight additions per thread fill the load/store queue and hold the
     // warps past the point where the next S^T and dP^T are ready (the chip
     // takes fp32 additions at about twice the rate this kernel issues them);
-    // spread out they drain while the exponentials run.  At d = 64 the extra
-    // sixteen registers spill, so it keeps the single burst.
-    constexpr bool kDefer = (D == 128) && !PAIR;
-    uint32_t pend[16];
+    // spread out they drain while the exponentials run.  At d = 64 even two
+    // deferred groups (eight registers) spill, so it keeps the single burst.
+    constexpr int kDeferG = (PAIR || D != 128) ? 0 : 4;  // deferred float4 groups
+    constexpr bool kDefer = kDeferG > 0;
+    uint32_t pend[kDefer ? 4 * kDeferG : 1];
     float4 *pend_dst = nullptr;
     bool ok = true;
     for (int t = 0; ok && t < n_steps; ++t) {
@@ -451,7 +452,9 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
         tmem_ld_wait(sr);
         tmem_ld_wait(dr);
         if constexpr (kDefer) {
-          if (pend_dst != nullptr) red_groups<2>(pend_dst + (4 + 2 * sc) * 128, pend + 8 * sc);
+          if (pend_dst != nullptr)
+            red_groups<kDeferG / 2>(pend_dst + (8 - kDeferG + (kDeferG / 2) * sc) * 128,
+                                    pend + 2 * kDeferG * sc);
           if (sc == 1) pend_dst = nullptr;
         }
         uint32_t pk[8], gk[8];
@@ -550,9 +553,9 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
             }
           }
         } else if (kDefer) {
-          red_groups<4>(dst, r);
+          red_groups<8 - kDeferG>(dst, r);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) pend[e] = r[16 + e];
+          for (int e = 0; e < 4 * kDeferG; ++e) pend[e] = r[4 * (8 - kDeferG) + e];
           pend_dst = dst;
         } else {
           red_groups<8>(dst, r);
@@ -565,7 +568,7 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       // same step as all the others
       if (PAIR && paired) ok = bar_and(1, 32 * C::kComputeWarps, ok);
     }
-    if (kDefer && pend_dst != nullptr) red_groups<4>(pend_dst + 4 * 128, pend);
+    if (kDefer && pend_dst != nullptr) red_groups<kDeferG>(pend_dst + (8 - kDeferG) * 128, pend);
     // epilogue: dK (times scale) and dV of this quadrant's keys; 32 columns
     // each: d = 128, slice cs of both; d = 64, slices 0-1 take dK and 2-3 dV
     ok = __all_sync(0xffffffffu, ok);
