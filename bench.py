@@ -76,7 +76,13 @@ METRIC = "attention fwd TFLOPS (bf16, 1×GB300) and fraction of dense tensor-cor
 METRIC_BWD = "attention bwd TFLOPS (bf16, 1×GB300) and fraction of dense tensor-core peak"
 DEFAULT_WORKLOAD = "b1h32n16384d128_causal"
 FALLBACK_BF16_TFLOPS = 1900.0
-KERNEL_SOURCES = ["fa_api.cu", "fa_kernel.cuh", "fa_bwd_kernel.cuh", "ptx.cuh"]
+# The library sources each profiled kernel is built from (its launch, its
+# device code and the PTX wrappers): a change to the backward's kernel file
+# leaves the forward's profiles valid.
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": ["fa_api.cu", "fa_kernel.cuh", "ptx.cuh"],
+    "fa_bwd_kernel": ["fa_api.cu", "fa_kernel.cuh", "fa_bwd_kernel.cuh", "ptx.cuh"],
+}
 AUTO_TIMED_S = 2.0  # timed work with no --steps
 SUSTAINED_AFTER_S = 1.0  # timed regions at least this long compare against the sustained peak
 CPU_SAMPLE_FLOP = 1.1e12  # oracle work of the default cpu_baseline sample (~17 s on 16 cores)
@@ -102,11 +108,11 @@ def _code_only(text: str) -> str:
     return "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
 
 
-def kernel_source_hash() -> str:
-    """Hash of the library's code (comments excluded): a profile taken at one
-    hash describes every source with the same hash."""
+def kernel_source_hash(kernel: str = "fa_fwd_kernel") -> str:
+    """Hash of the code `kernel` is built from (comments excluded): a profile
+    taken at one hash describes every source with the same hash."""
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "exact_attention_forward_07_gb300", "csrc", name)) as f:
             h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
@@ -122,7 +128,7 @@ def profiled_traffic(workload: str, kernel: str = "fa_fwd_kernel"):
         return None
     m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
     m_traffic = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not (m_hash and m_traffic) or m_hash.group(1) != kernel_source_hash():
+    if not (m_hash and m_traffic) or m_hash.group(1) != kernel_source_hash(kernel):
         return None
     return float(m_traffic.group(1))
 

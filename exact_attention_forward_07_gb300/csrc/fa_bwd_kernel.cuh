@@ -421,7 +421,8 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     const uint32_t peer_send_ok = PAIR ? mapa_shared(bar(C::bSendOk), rank ^ 1u) : 0u;
     const uint32_t peer_recv = PAIR ? mapa_shared(bar(C::bRecv), rank ^ 1u) : 0u;
     // d = 128: half of each step's dQ additions are deferred into the next
-    // step's softmax, two float4 groups per sub-chunk.  Issued all at once,
+    // step's softmax, one float4 group in every other of its eight slots
+    // (sub-chunk x group of four query columns).  Issued all at once,
     // the eight additions per thread fill the load/store queue and hold the
     // warps past the point where the next S^T and dP^T are ready (the chip
     // takes fp32 additions at about twice the rate this kernel issues them);
@@ -451,15 +452,17 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
         tmem_ld16(t_lane + C::cDP + q0, dr);
         tmem_ld_wait(sr);
         tmem_ld_wait(dr);
-        if constexpr (kDefer) {
-          if (pend_dst != nullptr)
-            red_groups<kDeferG / 2>(pend_dst + (8 - kDeferG + (kDeferG / 2) * sc) * 128,
-                                    pend + 2 * kDeferG * sc);
-          if (sc == 1) pend_dst = nullptr;
-        }
         uint32_t pk[8], gk[8];
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
+          if constexpr (kDefer) {
+            if (pend_dst != nullptr) {
+#pragma unroll
+              for (int k = 0; k < kDeferG; ++k)
+                if ((k * 8) / kDeferG == sc * 4 + e / 4)
+                  red_groups<1>(pend_dst + (8 - kDeferG + k) * 128, pend + 4 * k);
+            }
+          }
           const float4 l4 = *reinterpret_cast<const float4 *>(lse2s + q0 + e);
           const float4 d4 = *reinterpret_cast<const float4 *>(dds + q0 + e);
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
@@ -482,6 +485,7 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
         }
         // P^T of these 16 queries: 8 packed columns over this slice's own
         // S^T (columns 32 cs + 8 sc), already loaded
+        if (kDefer && sc == 1) pend_dst = nullptr;
         tmem_st8(t_lane + C::cS + 32 * cs + 8 * sc, pk);
         // dS^T: 32 bytes of the key's row, 16-byte chunks at their
         // 128-byte-swizzle positions

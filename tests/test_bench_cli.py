@@ -71,6 +71,7 @@ def test_kernel_hash_ignores_comments():
     assert bench._code_only(src) == bench._code_only(src.replace("note", "other note"))
     assert bench._code_only(src) != bench._code_only(src.replace("int b", "int c"))
     assert re.fullmatch(r"[0-9a-f]{16}", bench.kernel_source_hash())
+    assert bench.kernel_source_hash("fa_bwd_kernel") != bench.kernel_source_hash("fa_fwd_kernel")
 
 
 def test_clock_samples_kept_only_inside_the_timed_region():
