@@ -404,8 +404,9 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     // --------------------------------------------------------- compute warps
     // Sixteen warps; warp w owns the keys of lane quadrant w % 4 (one thread
     // per key) and the 32 query columns [32 cs, 32 cs + 32) of S^T, dP^T,
-    // P^T and dS^T, cs = (w - 4) / 4; then the same 32 columns of dQ for
-    // the query rows of its quadrant.  The two phases of a step never
+    // P^T and dS^T, cs = (w - 4) / 4; then columns [D cs / 4, D (cs + 1) / 4)
+    // of dQ for the query rows of its quadrant (32 columns at d = 128, 16 at
+    // d = 64; the CTA pairs keep 32, warps cs < 2 at d = 64).  The two phases of a step never
     // overlap (the next dP^T waits for dQ at d = 128), so one pool of warps
     // runs both, each on a quarter of the columns.
     const int w = warp - 4;
@@ -420,15 +421,19 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     const uint32_t peer_buf = PAIR ? mapa_shared(sbase + C::kDS, rank ^ 1u) : 0u;
     const uint32_t peer_send_ok = PAIR ? mapa_shared(bar(C::bSendOk), rank ^ 1u) : 0u;
     const uint32_t peer_recv = PAIR ? mapa_shared(bar(C::bRecv), rank ^ 1u) : 0u;
-    // d = 128: half of each step's dQ additions are deferred into the next
-    // step's softmax, one float4 group in every other of its eight slots
-    // (sub-chunk x group of four query columns).  Issued all at once,
-    // the eight additions per thread fill the load/store queue and hold the
-    // warps past the point where the next S^T and dP^T are ready (the chip
-    // takes fp32 additions at about twice the rate this kernel issues them);
-    // spread out they drain while the exponentials run.  At d = 64 even two
-    // deferred groups (eight registers) spill, so it keeps the single burst.
-    constexpr int kDeferG = (PAIR || D != 128) ? 0 : 4;  // deferred float4 groups
+    // Half of each step's dQ additions are deferred into the next step's
+    // softmax and spread over its eight slots (sub-chunk x group of four
+    // query columns).  Issued all at once, the additions fill the
+    // load/store queue and hold the warps past the point where the next S^T
+    // and dP^T are ready (the chip takes fp32 additions at about twice the
+    // rate this kernel issues them); spread out they drain while the
+    // exponentials run.
+    // dQ columns each warp reads out and adds: 32 (d = 128, and the CTA
+    // pairs' exchange layout), or 16 at d = 64, where all sixteen warps then
+    // share the read-out instead of eight
+    constexpr int kQC = (PAIR || D == 128) ? 32 : D / 4;
+    constexpr int kG = kQC / 4;  // their float4 groups
+    constexpr int kDeferG = PAIR ? 0 : kG / 2;  // deferred float4 groups
     constexpr bool kDefer = kDeferG > 0;
     uint32_t pend[kDefer ? 4 * kDeferG : 1];
     float4 *pend_dst = nullptr;
@@ -460,7 +465,7 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
 #pragma unroll
               for (int k = 0; k < kDeferG; ++k)
                 if ((k * 8) / kDeferG == sc * 4 + e / 4)
-                  red_groups<1>(pend_dst + (8 - kDeferG + k) * 128, pend + 4 * k);
+                  red_groups<1>(pend_dst + (kG - kDeferG + k) * 128, pend + 4 * k);
             }
           }
           const float4 l4 = *reinterpret_cast<const float4 *>(lse2s + q0 + e);
@@ -515,18 +520,23 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
         mbar_arrive_expect_tx(bar(C::bRecv), C::kRecvBytes);
         mbar_arrive_remote(peer_send_ok);
       }
-      uint32_t r[32];
-      if (32 * cs < D) {
-        tmem_ld32(t_lane + C::cDQ + 32 * cs, r);
+      uint32_t r[kQC];
+      if (kQC * cs < D) {
+        if constexpr (kQC == 32) {
+          tmem_ld32(t_lane + C::cDQ + kQC * cs, r);
+        } else {
+          tmem_ld16(t_lane + C::cDQ + kQC * cs, r);
+        }
         tmem_ld_wait(r);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::bDqFree));
-      if (32 * cs < D) {
+      if (kQC * cs < D) {
         float4 *dst = p.dq_acc + (static_cast<size_t>(bh) * T + i) * (D / 4) * 128 + row +
-                      8 * cs * 128;
-        if (PAIR && xchg) {
+                      kG * cs * 128;
+        if constexpr (PAIR) {
+        if (xchg) {
           // columns 32 cs + 16 k + [0, 16) belong to rank k: send the
           // peer's sixteen, then add the peer's to this CTA's own
           uint32_t mine[16], theirs[16];
@@ -556,13 +566,16 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
                          __uint_as_float(mine[4 * u + 3]) + x.w);
             }
           }
-        } else if (kDefer) {
-          red_groups<8 - kDeferG>(dst, r);
+        } else {
+          red_groups<kG>(dst, r);
+        }
+        } else if constexpr (kDefer) {
+          red_groups<kG - kDeferG>(dst, r);
 #pragma unroll
-          for (int e = 0; e < 4 * kDeferG; ++e) pend[e] = r[4 * (8 - kDeferG) + e];
+          for (int e = 0; e < 4 * kDeferG; ++e) pend[e] = r[4 * (kG - kDeferG) + e];
           pend_dst = dst;
         } else {
-          red_groups<8>(dst, r);
+          red_groups<kG>(dst, r);
         }
       }
       }
@@ -572,7 +585,7 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       // same step as all the others
       if (PAIR && paired) ok = bar_and(1, 32 * C::kComputeWarps, ok);
     }
-    if (kDefer && pend_dst != nullptr) red_groups<kDeferG>(pend_dst + (8 - kDeferG) * 128, pend);
+    if (kDefer && pend_dst != nullptr) red_groups<kDeferG>(pend_dst + (kG - kDeferG) * 128, pend);
     // epilogue: dK (times scale) and dV of this quadrant's keys; 32 columns
     // each: d = 128, slice cs of both; d = 64, slices 0-1 take dK and 2-3 dV
     ok = __all_sync(0xffffffffu, ok);
