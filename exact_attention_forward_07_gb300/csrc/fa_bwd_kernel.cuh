@@ -26,7 +26,8 @@
 // fa_bwd_kernel<PAIR = true> runs the same CTAs in clusters of two over
 // adjacent key blocks, which exchange halves of each dQ product through
 // distributed shared memory and so add half as many bytes to the fp32
-// accumulators (the additions, not the MMAs, bound the one-CTA kernel).
+// accumulators; the exchange ties the pair together on every step, and it
+// is slower than the one-CTA kernel.
 //
 // Roles in fa_bwd_kernel (640 threads):
 //   warp  0     TMA producer (one thread)
@@ -34,7 +35,8 @@
 //   warps 4-19  compute warps: warp w owns lane quadrant w % 4 and a slice
 //               of 32 columns; per step they form P^T and dS^T (one thread
 //               per key), then read dQ out of tensor memory (one thread per
-//               query row) and add it to the fp32 accumulators; at the end
+//               query row) and add it to the fp32 accumulators, half at once
+//               and half spread over the next step's softmax; at the end
 //               they write the block's dK and dV
 //
 // Per step (query block i):
@@ -404,11 +406,11 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     // --------------------------------------------------------- compute warps
     // Sixteen warps; warp w owns the keys of lane quadrant w % 4 (one thread
     // per key) and the 32 query columns [32 cs, 32 cs + 32) of S^T, dP^T,
-    // P^T and dS^T, cs = (w - 4) / 4; then columns [D cs / 4, D (cs + 1) / 4)
-    // of dQ for the query rows of its quadrant (32 columns at d = 128, 16 at
-    // d = 64; the CTA pairs keep 32, warps cs < 2 at d = 64).  The two phases of a step never
+    // P^T and dS^T, cs = (w - 4) / 4; then a quarter of dQ's columns for the
+    // query rows of its quadrant (32 at d = 128, 16 at d = 64; the CTA pairs
+    // read 32 with warps cs < 2 at d = 64).  The two phases of a step never
     // overlap (the next dP^T waits for dQ at d = 128), so one pool of warps
-    // runs both, each on a quarter of the columns.
+    // runs both.
     const int w = warp - 4;
     const int qd = w & 3, cs = w >> 2;
     const int row = qd * 32 + static_cast<int>(lane);  // key (phase 1) / query (phase 2)
@@ -421,16 +423,15 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     const uint32_t peer_buf = PAIR ? mapa_shared(sbase + C::kDS, rank ^ 1u) : 0u;
     const uint32_t peer_send_ok = PAIR ? mapa_shared(bar(C::bSendOk), rank ^ 1u) : 0u;
     const uint32_t peer_recv = PAIR ? mapa_shared(bar(C::bRecv), rank ^ 1u) : 0u;
-    // Half of each step's dQ additions are deferred into the next step's
-    // softmax and spread over its eight slots (sub-chunk x group of four
-    // query columns).  Issued all at once, the additions fill the
-    // load/store queue and hold the warps past the point where the next S^T
-    // and dP^T are ready (the chip takes fp32 additions at about twice the
-    // rate this kernel issues them); spread out they drain while the
-    // exponentials run.
     // dQ columns each warp reads out and adds: 32 (d = 128, and the CTA
     // pairs' exchange layout), or 16 at d = 64, where all sixteen warps then
-    // share the read-out instead of eight
+    // share the read-out instead of eight.  Half of each step's additions
+    // are deferred into the next step's softmax and spread over its eight
+    // slots (sub-chunk x group of four query columns).  Issued all at once,
+    // the additions fill the load/store queue and hold the warps past the
+    // point where the next S^T and dP^T are ready (the chip takes fp32
+    // additions at about twice the rate this kernel issued them); spread out
+    // they drain while the exponentials run.
     constexpr int kQC = (PAIR || D == 128) ? 32 : D / 4;
     constexpr int kG = kQC / 4;  // their float4 groups
     constexpr int kDeferG = PAIR ? 0 : kG / 2;  // deferred float4 groups
