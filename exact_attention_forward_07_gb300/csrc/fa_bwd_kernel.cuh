@@ -43,9 +43,10 @@
 //   S^T  = K_j Q_i^T      SS  -> TMEM [0,128)     (lanes = keys)
 //   dP^T = V_j dO_i^T     SS  -> TMEM [128,256)
 //   compute warps: P^T = 2^(S^T scale log2e - lse2_i), packed to 16 bits over
-//   S^T; dS^T = P^T (dP^T - D_i) to shared memory, 128-byte swizzled
-//   dV  += P^T dO_i       TS  (P^T from TMEM, dO_i MN-major)
-//   dK  += dS^T Q_i       SS  (dS^T K-major, Q_i MN-major)
+//   S^T; dS^T = P^T (dP^T - D_i) to shared memory, 128-byte swizzled; one
+//   query half at a time
+//   dV  += P^T dO_i       TS  (P^T from TMEM, dO_i MN-major), per query half
+//   dK  += dS^T Q_i       SS  (dS^T K-major, Q_i MN-major), per query half
 //   dQ_i = dS K_j         SS  (the same dS buffer read MN-major, K_j MN-major)
 // The dS buffer [query half][128 key rows][128 bytes] is at once the
 // K-major layout of dS^T (rows = keys) and the MN-major layout of dS (64
@@ -95,12 +96,13 @@ struct BwdCfg {
   static constexpr int kBar = kDd + 2 * 512;
   // barriers: K/V loaded; Q/dO stage full (2) and empty (2); S^T and dP^T
   // done; dS written and dQ read (one arrival per compute warp each); dQ
-  // done; dK/dV done; drain; and for CTA pairs: the peer may write into
-  // this CTA's dS buffer (arrived by the peer), the peer's dQ columns have
-  // landed there (one local arrival + the bytes)
+  // done; dK/dV done; drain; for CTA pairs: the peer may write into this
+  // CTA's dS buffer (arrived by the peer), the peer's dQ columns have landed
+  // there (one local arrival + the bytes); and the first half of the query
+  // columns' P^T and dS^T written (one arrival per compute warp)
   static constexpr int bKV = 0, bFull = 1, bEmpty = 3, bSdp = 5, bDs = 6, bDqFull = 7,
                        bDqFree = 8, bDkdv = 9, bDrain = 10, bSendOk = 11, bRecv = 12,
-                       kNumBars = 13;
+                       bDsA = 13, kNumBars = 14;
   static constexpr uint32_t kRecvBytes = 128 * (D / 2) * 4;  // half of dQ's columns, fp32
   static constexpr int kMisc = kBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kUsed = kMisc + 16;
@@ -284,6 +286,7 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     }
     mbar_init(bar(C::bSdp), 1);
     mbar_init(bar(C::bDs), C::kComputeWarps);      // one arrival per compute warp
+    mbar_init(bar(C::bDsA), C::kComputeWarps);     // the same, first query half
     mbar_init(bar(C::bDqFull), 1);
     mbar_init(bar(C::bDqFree), C::kComputeWarps);  // one arrival per compute warp
     mbar_init(bar(C::bDkdv), 1);
@@ -372,21 +375,26 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       }
       ss_kk(C::cDP, sbase + C::kV, do_s, C::kIdescS, D / 16, false);   // dP^T = V dO^T
       mma_commit_if(leader, bar(C::bSdp));
-      if (!(ok = wait_bar(bar(C::bDs), t & 1u, abort_flag, p.status))) break;
-      tc_fence_after();
-      // dV += P^T dO: P^T packed in tensor memory, query slice c (32
-      // queries) at columns [32c, 32c + 16)
+      // dV += P^T dO and dK += dS^T Q, K = the 128 queries, one half of them
+      // at a time: the first half's products run while the compute warps
+      // form the second half.  P^T of queries [16 kk, 16 kk + 16) is packed
+      // in tensor-memory columns [16 kk, 16 kk + 8); dS^T is K-major in
+      // shared memory; dO and Q are MN-major.
       const uint64_t bdo = mdesc0 + desc_addr(do_s), bq = mdesc0 + desc_addr(q_s);
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ts_if(leader, tmem + C::cDV, tmem + C::cS + 32 * (kk >> 1) + 8 * (kk & 1),
-                  bdo + kk * (2048 >> 4), C::kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
-      // dK += dS^T Q: dS^T K-major in shared memory, Q MN-major
       const uint64_t ads = kdesc0 + desc_addr(sbase + C::kDS);
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;
-        mma_ss_if(leader, tmem + C::cDK, ads + off, bq + kk * (2048 >> 4), C::kIdescG,
-                  (t > 0 || kk > 0) ? 1u : 0u);
+      for (int hq = 0; hq < 2 && ok; ++hq) {
+        if (!(ok = wait_bar(bar(hq ? C::bDs : C::bDsA), t & 1u, abort_flag, p.status))) break;
+        tc_fence_after();
+        for (int kk = 4 * hq; kk < 4 * hq + 4; ++kk)
+          mma_ts_if(leader, tmem + C::cDV, tmem + C::cS + 16 * kk, bdo + kk * (2048 >> 4),
+                    C::kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 4 * hq; kk < 4 * hq + 4; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;
+          mma_ss_if(leader, tmem + C::cDK, ads + off, bq + kk * (2048 >> 4), C::kIdescG,
+                    (t > 0 || kk > 0) ? 1u : 0u);
+        }
       }
+      if (!ok) break;
       if (!C::kDqAliasDp && t > 0) {  // dQ(t-1) read out of its own columns
         if (!(ok = wait_bar(bar(C::bDqFree), (t - 1) & 1u, abort_flag, p.status))) break;
         tc_fence_after();
@@ -405,8 +413,10 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
   } else if (warp >= 4 && !idle) {
     // --------------------------------------------------------- compute warps
     // Sixteen warps; warp w owns the keys of lane quadrant w % 4 (one thread
-    // per key) and the 32 query columns [32 cs, 32 cs + 32) of S^T, dP^T,
-    // P^T and dS^T, cs = (w - 4) / 4; then a quarter of dQ's columns for the
+    // per key) and the query columns [16 cs, 16 cs + 16) of each query half
+    // (cs = (w - 4) / 4) of S^T, dP^T, P^T and dS^T, the first half before
+    // the second, so that the first half's dV and dK products overlap the
+    // second half's softmax; then a quarter of dQ's columns for the
     // query rows of its quadrant (32 at d = 128, 16 at d = 64; the CTA pairs
     // read 32 with warps cs < 2 at d = 64).  The two phases of a step never
     // overlap (the next dP^T waits for dQ at d = 128), so one pool of warps
@@ -417,8 +427,6 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     const bool key_dead = jb * 128 + row >= p.N;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(qd * 32) << 16);
     const uint64_t sl2_2 = f2(p.scale_log2, p.scale_log2);
-    // this key's 128-byte row of dS^T in half cs / 2 of the query columns
-    uint8_t *ds_row = smem + C::kDS + (cs >> 1) * C::kHalf + row * 128;
     // PAIR: the peer's dS buffer and barriers, as seen from this CTA
     const uint32_t peer_buf = PAIR ? mapa_shared(sbase + C::kDS, rank ^ 1u) : 0u;
     const uint32_t peer_send_ok = PAIR ? mapa_shared(bar(C::bSendOk), rank ^ 1u) : 0u;
@@ -452,7 +460,7 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       const bool diag = p.causal && i == jb;
 #pragma unroll
       for (int sc = 0; sc < 2; ++sc) {
-        const int q0 = 32 * cs + 16 * sc;  // first query column of this sub-chunk
+        const int q0 = 16 * cs + 64 * sc;  // first query column of this sub-chunk
         uint32_t sr[16], dr[16];
         tmem_ld16(t_lane + C::cS + q0, sr);
         tmem_ld16(t_lane + C::cDP + q0, dr);
@@ -489,17 +497,25 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
             gk[(e + u) >> 1] = pack2<BF16>(g0, g1);
           }
         }
-        // P^T of these 16 queries: 8 packed columns over this slice's own
-        // S^T (columns 32 cs + 8 sc), already loaded
+        // P^T of these 16 queries: 8 packed columns over their own S^T
+        // columns, already loaded
         if (kDefer && sc == 1) pend_dst = nullptr;
-        tmem_st8(t_lane + C::cS + 32 * cs + 8 * sc, pk);
-        // dS^T: 32 bytes of the key's row, 16-byte chunks at their
-        // 128-byte-swizzle positions
+        tmem_st8(t_lane + C::cS + q0, pk);
+        // dS^T: 32 bytes of the key's row in query half sc, 16-byte chunks
+        // at their 128-byte-swizzle positions
+        uint8_t *ds_row = smem + C::kDS + sc * C::kHalf + row * 128;
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const int pos = (4 * (cs & 1) + 2 * sc + u) ^ (row & 7);
+          const int pos = (2 * cs + u) ^ (row & 7);
           *reinterpret_cast<uint4 *>(ds_row + 16 * pos) =
               make_uint4(gk[4 * u], gk[4 * u + 1], gk[4 * u + 2], gk[4 * u + 3]);
+        }
+        if (sc == 0) {  // the first query half of P^T and dS^T is complete
+          tmem_st_wait();
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(C::bDsA));
         }
       }
       tmem_st_wait();
