@@ -47,7 +47,8 @@
 //   query half at a time
 //   dV  += P^T dO_i       TS  (P^T from TMEM, dO_i MN-major), per query half
 //   dK  += dS^T Q_i       SS  (dS^T K-major, Q_i MN-major), per query half
-//   dQ_i = dS K_j         SS  (the same dS buffer read MN-major, K_j MN-major)
+//   dQ_i = dS K_j         SS  (the same dS buffer read MN-major, K_j MN-major),
+//                             between the two halves' dV and dK
 // The dS buffer [query half][128 key rows][128 bytes] is at once the
 // K-major layout of dS^T (rows = keys) and the MN-major layout of dS (64
 // queries per swizzled row, keys along the rows), so one store serves both
@@ -382,9 +383,28 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       // shared memory; dO and Q are MN-major.
       const uint64_t bdo = mdesc0 + desc_addr(do_s), bq = mdesc0 + desc_addr(q_s);
       const uint64_t ads = kdesc0 + desc_addr(sbase + C::kDS);
+      // dQ = dS K: the same buffer read MN-major, K MN-major.  It needs all
+      // of dS, and goes first once dS is complete (before the second half
+      // of dV and dK), so the compute warps' read-out of dQ and the next
+      // step's dP^T start sooner.  The CTA pairs issue it last: their
+      // "dQ done" must also mean that dK has finished reading dS.
+      auto issue_dq = [&]() -> bool {
+        if (!C::kDqAliasDp && t > 0) {  // dQ(t-1) read out of its own columns
+          if (!wait_bar(bar(C::bDqFree), (t - 1) & 1u, abort_flag, p.status)) return false;
+          tc_fence_after();
+        }
+        const uint64_t adt = mdesc0 + desc_addr(sbase + C::kDS);
+        const uint64_t bk = mdesc0 + desc_addr(sbase + C::kK);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss_if(leader, tmem + C::cDQ, adt + kk * (2048 >> 4), bk + kk * (2048 >> 4),
+                    C::kIdescQ, kk > 0 ? 1u : 0u);
+        mma_commit_if(leader, bar(C::bDqFull));
+        return true;
+      };
       for (int hq = 0; hq < 2 && ok; ++hq) {
         if (!(ok = wait_bar(bar(hq ? C::bDs : C::bDsA), t & 1u, abort_flag, p.status))) break;
         tc_fence_after();
+        if (!PAIR && hq == 1 && !(ok = issue_dq())) break;
         for (int kk = 4 * hq; kk < 4 * hq + 4; ++kk)
           mma_ts_if(leader, tmem + C::cDV, tmem + C::cS + 16 * kk, bdo + kk * (2048 >> 4),
                     C::kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
@@ -395,17 +415,8 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
         }
       }
       if (!ok) break;
-      if (!C::kDqAliasDp && t > 0) {  // dQ(t-1) read out of its own columns
-        if (!(ok = wait_bar(bar(C::bDqFree), (t - 1) & 1u, abort_flag, p.status))) break;
-        tc_fence_after();
-      }
-      // dQ = dS K: the same buffer read MN-major, K MN-major
-      const uint64_t adt = mdesc0 + desc_addr(sbase + C::kDS), bk = mdesc0 + desc_addr(sbase + C::kK);
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ss_if(leader, tmem + C::cDQ, adt + kk * (2048 >> 4), bk + kk * (2048 >> 4), C::kIdescQ,
-                  kk > 0 ? 1u : 0u);
-      mma_commit_if(leader, bar(C::bDqFull));
-      mma_commit_if(leader, bar(C::bEmpty + s));
+      if (PAIR && !(ok = issue_dq())) break;
+      mma_commit_if(leader, bar(C::bEmpty + s));  // Q and dO of this stage read
     }
     if (ok) mma_commit_if(leader, bar(C::bDkdv));
     mma_commit_if(leader, bar(C::bDrain));
