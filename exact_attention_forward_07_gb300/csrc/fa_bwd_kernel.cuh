@@ -203,6 +203,12 @@ __global__ void __launch_bounds__(128) fa_bwd_dq_kernel(const BwdParams p) {
   }
 }
 
+// A compile-time bool as a value, for generic lambdas.
+template <bool B>
+struct BoolTag {
+  static constexpr bool value = B;
+};
+
 // NG groups of four fp32 additions: v[4u .. 4u + 3] into dst[128 u], the
 // accumulator layout's float4 columns of one row.
 template <int NG>
@@ -469,6 +475,7 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       const float *lse2s = reinterpret_cast<const float *>(smem + C::kLse + s * 512);
       const float *dds = reinterpret_cast<const float *>(smem + C::kDd + s * 512);
       const bool diag = p.causal && i == jb;
+      const bool masked = diag || (jb + 1) * 128 > p.N;
 #pragma unroll
       for (int sc = 0; sc < 2; ++sc) {
         const int q0 = 16 * cs + 64 * sc;  // first query column of this sub-chunk
@@ -478,35 +485,48 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
         tmem_ld_wait(sr);
         tmem_ld_wait(dr);
         uint32_t pk[8], gk[8];
+        // P^T and dS^T of these 16 queries; MASK: the step needs the causal
+        // diagonal or has keys past N (both uniform over the CTA), so the
+        // other steps run without the per-element selects
+        auto form = [&](auto mask_tag) {
+          constexpr bool MASK = decltype(mask_tag)::value;
 #pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          if constexpr (kDefer) {
-            if (pend_dst != nullptr) {
+          for (int e = 0; e < 16; e += 4) {
+            if constexpr (kDefer) {
+              if (pend_dst != nullptr) {
 #pragma unroll
-              for (int k = 0; k < kDeferG; ++k)
-                if ((k * 8) / kDeferG == sc * 4 + e / 4)
-                  red_groups<1>(pend_dst + (kG - kDeferG + k) * 128, pend + 4 * k);
+                for (int k = 0; k < kDeferG; ++k)
+                  if ((k * 8) / kDeferG == sc * 4 + e / 4)
+                    red_groups<1>(pend_dst + (kG - kDeferG + k) * 128, pend + 4 * k);
+              }
+            }
+            const float4 l4 = *reinterpret_cast<const float4 *>(lse2s + q0 + e);
+            const float4 d4 = *reinterpret_cast<const float4 *>(dds + q0 + e);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+            for (int u = 0; u < 4; u += 2) {
+              float x0, x1;
+              f2_split(ffma2(f2(__uint_as_float(sr[e + u]), __uint_as_float(sr[e + u + 1])), sl2_2,
+                             f2(-lv[u], -lv[u + 1])),
+                       x0, x1);
+              float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              if constexpr (MASK) {
+                if (key_dead || (diag && row > q0 + e + u)) p0 = 0.f;
+                if (key_dead || (diag && row > q0 + e + u + 1)) p1 = 0.f;
+              }
+              float g0, g1;
+              f2_split(fmul2(f2(p0, p1), fadd2(f2(__uint_as_float(dr[e + u]), __uint_as_float(dr[e + u + 1])),
+                                               f2(-dv[u], -dv[u + 1]))),
+                       g0, g1);
+              pk[(e + u) >> 1] = pack2<BF16>(p0, p1);
+              gk[(e + u) >> 1] = pack2<BF16>(g0, g1);
             }
           }
-          const float4 l4 = *reinterpret_cast<const float4 *>(lse2s + q0 + e);
-          const float4 d4 = *reinterpret_cast<const float4 *>(dds + q0 + e);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-          for (int u = 0; u < 4; u += 2) {
-            float x0, x1;
-            f2_split(ffma2(f2(__uint_as_float(sr[e + u]), __uint_as_float(sr[e + u + 1])), sl2_2,
-                           f2(-lv[u], -lv[u + 1])),
-                     x0, x1);
-            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            if (key_dead || (diag && row > q0 + e + u)) p0 = 0.f;
-            if (key_dead || (diag && row > q0 + e + u + 1)) p1 = 0.f;
-            float g0, g1;
-            f2_split(fmul2(f2(p0, p1), fadd2(f2(__uint_as_float(dr[e + u]), __uint_as_float(dr[e + u + 1])),
-                                             f2(-dv[u], -dv[u + 1]))),
-                     g0, g1);
-            pk[(e + u) >> 1] = pack2<BF16>(p0, p1);
-            gk[(e + u) >> 1] = pack2<BF16>(g0, g1);
-          }
+        };
+        if (masked) {
+          form(BoolTag<true>{});
+        } else {
+          form(BoolTag<false>{});
         }
         // P^T of these 16 queries: 8 packed columns over their own S^T
         // columns, already loaded
