@@ -100,10 +100,11 @@ struct BwdCfg {
   // done; dK/dV done; drain; for CTA pairs: the peer may write into this
   // CTA's dS buffer (arrived by the peer), the peer's dQ columns have landed
   // there (one local arrival + the bytes); and the first half of the query
-  // columns' P^T and dS^T written (one arrival per compute warp)
+  // columns' P^T and dS^T written (one arrival per compute warp); and (d =
+  // 64) a step's second-half dV and dK done (an MMA commit)
   static constexpr int bKV = 0, bFull = 1, bEmpty = 3, bSdp = 5, bDs = 6, bDqFull = 7,
                        bDqFree = 8, bDkdv = 9, bDrain = 10, bSendOk = 11, bRecv = 12,
-                       bDsA = 13, kNumBars = 14;
+                       bDsA = 13, bTail = 14, kNumBars = 15;
   static constexpr uint32_t kRecvBytes = 128 * (D / 2) * 4;  // half of dQ's columns, fp32
   static constexpr int kMisc = kBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kUsed = kMisc + 16;
@@ -117,6 +118,9 @@ struct BwdCfg {
   static constexpr bool kDqAliasDp = (D == 128);
   static constexpr uint32_t cS = 0, cDP = 128, cDK = 256, cDV = 256 + D;
   static constexpr uint32_t cDQ = kDqAliasDp ? cDP : 256 + 2 * D;
+  // d = 64: the second query half's P^T in columns of its own (the last
+  // 64 are free), so the next step's S^T may overwrite S while it waits
+  static constexpr uint32_t cP2 = 256 + 3 * D;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kIdescS = idesc_f16(BF16, false, 128, 128);         // S^T, dP^T
   static constexpr uint32_t kIdescG = idesc_f16(BF16, true, 128, D);            // dV, dK
@@ -253,6 +257,13 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdParams p) {
   using C = BwdCfg<D, BF16>;
+  // d = 64 (one CTA per key block): steps overlap.  With the second query
+  // half's P^T in its own tensor-memory columns, the next step's S^T and
+  // dP^T go to the tensor core as soon as this step's dS is complete, ahead
+  // of this step's dQ and second-half dV and dK, and the compute warps form
+  // the next step's P^T and dS^T while those run; they read out this
+  // step's dQ after that.
+  constexpr bool kPipe = (D == 64) && !PAIR;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -294,6 +305,7 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     mbar_init(bar(C::bSdp), 1);
     mbar_init(bar(C::bDs), C::kComputeWarps);      // one arrival per compute warp
     mbar_init(bar(C::bDsA), C::kComputeWarps);     // the same, first query half
+    mbar_init(bar(C::bTail), 1);
     mbar_init(bar(C::bDqFull), 1);
     mbar_init(bar(C::bDqFree), C::kComputeWarps);  // one arrival per compute warp
     mbar_init(bar(C::bDkdv), 1);
@@ -370,6 +382,58 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       }
     };
     bool ok = wait_bar(bar(C::bKV), 0, abort_flag, p.status);
+    if constexpr (kPipe) {
+      // S^T(t) and dP^T(t) of a step, once its Q and dO are loaded
+      auto issue_sdp = [&](int tt) -> bool {
+        const int st = tt & 1;
+        if (!wait_bar(bar(C::bFull + st), (tt >> 1) & 1u, abort_flag, p.status)) return false;
+        tc_fence_after();
+        ss_kk(C::cS, sbase + C::kK, sbase + C::kQ + st * C::kTile, C::kIdescS, D / 16, false);
+        ss_kk(C::cDP, sbase + C::kV, sbase + C::kDO + st * C::kTile, C::kIdescS, D / 16, false);
+        mma_commit_if(leader, bar(C::bSdp));
+        return true;
+      };
+      if (ok && n_steps > 0) ok = issue_sdp(0);
+      for (int t = 0; ok && t < n_steps; ++t) {
+        const int s = t & 1;
+        const uint32_t q_s = sbase + C::kQ + s * C::kTile, do_s = sbase + C::kDO + s * C::kTile;
+        const uint64_t bdo = mdesc0 + desc_addr(do_s), bq = mdesc0 + desc_addr(q_s);
+        const uint64_t ads = kdesc0 + desc_addr(sbase + C::kDS);
+        // first query half: P^T in S's columns
+        if (!(ok = wait_bar(bar(C::bDsA), t & 1u, abort_flag, p.status))) break;
+        tc_fence_after();
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts_if(leader, tmem + C::cDV, tmem + C::cS + 16 * kk, bdo + kk * (2048 >> 4),
+                    C::kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss_if(leader, tmem + C::cDK, ads + ((kk * 32) >> 4), bq + kk * (2048 >> 4),
+                    C::kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
+        if (!(ok = wait_bar(bar(C::bDs), t & 1u, abort_flag, p.status))) break;
+        tc_fence_after();
+        // the next step's S^T (S is free: the first half's dV above read
+        // its P^T) and dP^T (read by this step's softmax)
+        if (t + 1 < n_steps && !(ok = issue_sdp(t + 1))) break;
+        if (t > 0) {  // dQ(t-1) read out of its columns
+          if (!(ok = wait_bar(bar(C::bDqFree), (t - 1) & 1u, abort_flag, p.status))) break;
+          tc_fence_after();
+        }
+        const uint64_t adt = mdesc0 + desc_addr(sbase + C::kDS);
+        const uint64_t bk = mdesc0 + desc_addr(sbase + C::kK);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss_if(leader, tmem + C::cDQ, adt + kk * (2048 >> 4), bk + kk * (2048 >> 4),
+                    C::kIdescQ, kk > 0 ? 1u : 0u);
+        mma_commit_if(leader, bar(C::bDqFull));
+        // second query half: P^T in its own columns
+        for (int kk = 4; kk < 8; ++kk)
+          mma_ts_if(leader, tmem + C::cDV, tmem + C::cP2 + 8 * (kk - 4), bdo + kk * (2048 >> 4),
+                    C::kIdescG, 1u);
+        for (int kk = 4; kk < 8; ++kk)
+          mma_ss_if(leader, tmem + C::cDK, ads + ((C::kHalf + (kk & 3) * 32) >> 4),
+                    bq + kk * (2048 >> 4), C::kIdescG, 1u);
+        mma_commit_if(leader, bar(C::bTail));       // its P^T columns and dS half free
+        mma_commit_if(leader, bar(C::bEmpty + s));  // Q and dO of this stage read
+      }
+    } else {
     for (int t = 0; ok && t < n_steps; ++t) {
       const int s = t & 1;
       const uint32_t q_s = sbase + C::kQ + s * C::kTile, do_s = sbase + C::kDO + s * C::kTile;
@@ -424,6 +488,7 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       if (PAIR && !(ok = issue_dq())) break;
       mma_commit_if(leader, bar(C::bEmpty + s));  // Q and dO of this stage read
     }
+    }
     if (ok) mma_commit_if(leader, bar(C::bDkdv));
     mma_commit_if(leader, bar(C::bDrain));
     wait_drain(bar(C::bDrain), 0, abort_flag, p.status);
@@ -463,105 +528,16 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     constexpr bool kDefer = kDeferG > 0;
     uint32_t pend[kDefer ? 4 * kDeferG : 1];
     float4 *pend_dst = nullptr;
-    bool ok = true;
-    for (int t = 0; ok && t < n_steps; ++t) {
-      // query block shared with the peer: every warp takes the same branch
-      const bool xchg = paired && t >= xs0;
-      const uint32_t xpar = static_cast<uint32_t>(t - xs0) & 1u;
-      ok = wait_bar(bar(C::bSdp), t & 1u, abort_flag, p.status);
+    // Phase 2 of step tt: its dQ (query rows of this quadrant) into
+    // registers; the tensor-memory columns are released before the
+    // additions are issued, so the next MMAs overlap them.
+    auto phase2 = [&](int tt) -> bool {
+      const bool xchg = paired && tt >= xs0;
+      const uint32_t xpar = static_cast<uint32_t>(tt - xs0) & 1u;
+      bool ok = wait_bar(bar(C::bDqFull), tt & 1u, abort_flag, p.status);
       if (ok) {
       tc_fence_after();
-      const int s = t & 1, i = i0 + t;
-      const float *lse2s = reinterpret_cast<const float *>(smem + C::kLse + s * 512);
-      const float *dds = reinterpret_cast<const float *>(smem + C::kDd + s * 512);
-      const bool diag = p.causal && i == jb;
-      const bool masked = diag || (jb + 1) * 128 > p.N;
-#pragma unroll
-      for (int sc = 0; sc < 2; ++sc) {
-        const int q0 = 16 * cs + 64 * sc;  // first query column of this sub-chunk
-        uint32_t sr[16], dr[16];
-        tmem_ld16(t_lane + C::cS + q0, sr);
-        tmem_ld16(t_lane + C::cDP + q0, dr);
-        tmem_ld_wait(sr);
-        tmem_ld_wait(dr);
-        uint32_t pk[8], gk[8];
-        // P^T and dS^T of these 16 queries; MASK: the step needs the causal
-        // diagonal or has keys past N (both uniform over the CTA), so the
-        // other steps run without the per-element selects
-        auto form = [&](auto mask_tag) {
-          constexpr bool MASK = decltype(mask_tag)::value;
-#pragma unroll
-          for (int e = 0; e < 16; e += 4) {
-            if constexpr (kDefer) {
-              if (pend_dst != nullptr) {
-#pragma unroll
-                for (int k = 0; k < kDeferG; ++k)
-                  if ((k * 8) / kDeferG == sc * 4 + e / 4)
-                    red_groups<1>(pend_dst + (kG - kDeferG + k) * 128, pend + 4 * k);
-              }
-            }
-            const float4 l4 = *reinterpret_cast<const float4 *>(lse2s + q0 + e);
-            const float4 d4 = *reinterpret_cast<const float4 *>(dds + q0 + e);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-            for (int u = 0; u < 4; u += 2) {
-              float x0, x1;
-              f2_split(ffma2(f2(__uint_as_float(sr[e + u]), __uint_as_float(sr[e + u + 1])), sl2_2,
-                             f2(-lv[u], -lv[u + 1])),
-                       x0, x1);
-              float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-              if constexpr (MASK) {
-                if (key_dead || (diag && row > q0 + e + u)) p0 = 0.f;
-                if (key_dead || (diag && row > q0 + e + u + 1)) p1 = 0.f;
-              }
-              float g0, g1;
-              f2_split(fmul2(f2(p0, p1), fadd2(f2(__uint_as_float(dr[e + u]), __uint_as_float(dr[e + u + 1])),
-                                               f2(-dv[u], -dv[u + 1]))),
-                       g0, g1);
-              pk[(e + u) >> 1] = pack2<BF16>(p0, p1);
-              gk[(e + u) >> 1] = pack2<BF16>(g0, g1);
-            }
-          }
-        };
-        if (masked) {
-          form(BoolTag<true>{});
-        } else {
-          form(BoolTag<false>{});
-        }
-        // P^T of these 16 queries: 8 packed columns over their own S^T
-        // columns, already loaded
-        if (kDefer && sc == 1) pend_dst = nullptr;
-        tmem_st8(t_lane + C::cS + q0, pk);
-        // dS^T: 32 bytes of the key's row in query half sc, 16-byte chunks
-        // at their 128-byte-swizzle positions
-        uint8_t *ds_row = smem + C::kDS + sc * C::kHalf + row * 128;
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int pos = (2 * cs + u) ^ (row & 7);
-          *reinterpret_cast<uint4 *>(ds_row + 16 * pos) =
-              make_uint4(gk[4 * u], gk[4 * u + 1], gk[4 * u + 2], gk[4 * u + 3]);
-        }
-        if (sc == 0) {  // the first query half of P^T and dS^T is complete
-          tmem_st_wait();
-          fence_proxy_async_smem();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(C::bDsA));
-        }
-      }
-      tmem_st_wait();
-      fence_proxy_async_smem();  // dS^T stores visible to the tensor core
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::bDs));
-      }
-      // phase 2: dQ of this step (query rows of this quadrant, 32 columns)
-      // into registers; its tensor-memory columns are released before the
-      // additions are issued, so the next step's MMAs overlap them
-      if (ok) ok = wait_bar(bar(C::bDqFull), t & 1u, abort_flag, p.status);
-      if (ok) {
-      tc_fence_after();
-      const int i = i0 + t;
+      const int i = i0 + tt;
       if (PAIR && xchg && w == 0 && lane == 0) {
         // this CTA's dK and dQ MMAs have read its dS buffer: the peer may
         // write its columns there
@@ -627,12 +603,128 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
         }
       }
       }
+      return ok;
+    };
+    bool ok = true;
+    for (int t = 0; ok && t < n_steps; ++t) {
+      ok = wait_bar(bar(C::bSdp), t & 1u, abort_flag, p.status);
+      if (ok) {
+      tc_fence_after();
+      const int s = t & 1, i = i0 + t;
+      const float *lse2s = reinterpret_cast<const float *>(smem + C::kLse + s * 512);
+      const float *dds = reinterpret_cast<const float *>(smem + C::kDd + s * 512);
+      const bool diag = p.causal && i == jb;
+      const bool masked = diag || (jb + 1) * 128 > p.N;
+#pragma unroll
+      for (int sc = 0; sc < 2; ++sc) {
+        const int q0 = 16 * cs + 64 * sc;  // first query column of this sub-chunk
+        uint32_t sr[16], dr[16];
+        tmem_ld16(t_lane + C::cS + q0, sr);
+        tmem_ld16(t_lane + C::cDP + q0, dr);
+        tmem_ld_wait(sr);
+        tmem_ld_wait(dr);
+        uint32_t pk[8], gk[8];
+        // P^T and dS^T of these 16 queries; MASK: the step needs the causal
+        // diagonal or has keys past N (both uniform over the CTA), so the
+        // other steps run without the per-element selects
+        auto form = [&](auto mask_tag) {
+          constexpr bool MASK = decltype(mask_tag)::value;
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) {
+            if constexpr (kDefer) {
+              if (pend_dst != nullptr) {
+#pragma unroll
+                for (int k = 0; k < kDeferG; ++k)
+                  if ((k * 8) / kDeferG == sc * 4 + e / 4)
+                    red_groups<1>(pend_dst + (kG - kDeferG + k) * 128, pend + 4 * k);
+              }
+            }
+            const float4 l4 = *reinterpret_cast<const float4 *>(lse2s + q0 + e);
+            const float4 d4 = *reinterpret_cast<const float4 *>(dds + q0 + e);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+            for (int u = 0; u < 4; u += 2) {
+              float x0, x1;
+              f2_split(ffma2(f2(__uint_as_float(sr[e + u]), __uint_as_float(sr[e + u + 1])), sl2_2,
+                             f2(-lv[u], -lv[u + 1])),
+                       x0, x1);
+              float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              if constexpr (MASK) {
+                if (key_dead || (diag && row > q0 + e + u)) p0 = 0.f;
+                if (key_dead || (diag && row > q0 + e + u + 1)) p1 = 0.f;
+              }
+              float g0, g1;
+              f2_split(fmul2(f2(p0, p1), fadd2(f2(__uint_as_float(dr[e + u]), __uint_as_float(dr[e + u + 1])),
+                                               f2(-dv[u], -dv[u + 1]))),
+                       g0, g1);
+              pk[(e + u) >> 1] = pack2<BF16>(p0, p1);
+              gk[(e + u) >> 1] = pack2<BF16>(g0, g1);
+            }
+          }
+        };
+        if (masked) {
+          form(BoolTag<true>{});
+        } else {
+          form(BoolTag<false>{});
+        }
+        // kPipe: the previous step's dQ has read dS half 0 (and its
+        // first-half dK before it), and its second-half dV and dK have read
+        // P^T's own columns and dS half 1, before this step writes them
+        if constexpr (kPipe) {
+          if (t > 0 && !wait_bar(bar(sc ? C::bTail : C::bDqFull), (t - 1) & 1u, abort_flag,
+                                 p.status))
+            ok = false;
+          tc_fence_after();
+        }
+        // P^T of these 16 queries: 8 packed columns over their own S^T
+        // columns, already loaded (kPipe: the second half in its own columns)
+        if (kDefer && sc == 1) pend_dst = nullptr;
+        if (kPipe && sc == 1) {
+          tmem_st8(t_lane + C::cP2 + 8 * cs, pk);
+        } else {
+          tmem_st8(t_lane + C::cS + q0, pk);
+        }
+        // dS^T: 32 bytes of the key's row in query half sc, 16-byte chunks
+        // at their 128-byte-swizzle positions
+        uint8_t *ds_row = smem + C::kDS + sc * C::kHalf + row * 128;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int pos = (2 * cs + u) ^ (row & 7);
+          *reinterpret_cast<uint4 *>(ds_row + 16 * pos) =
+              make_uint4(gk[4 * u], gk[4 * u + 1], gk[4 * u + 2], gk[4 * u + 3]);
+        }
+        if (sc == 0) {  // the first query half of P^T and dS^T is complete
+          tmem_st_wait();
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(C::bDsA));
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();  // dS^T stores visible to the tensor core
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::bDs));
+      }
+      if (ok) {
+        if constexpr (kPipe) {
+          if (t > 0) ok = phase2(t - 1);  // the previous step's dQ, read out behind this softmax
+        } else {
+          ok = phase2(t);
+        }
+      }
       // PAIR: no compute warp writes the next dS before all have read the
       // peer's columns out of the same buffer; taken on every step of a
       // paired CTA, so that a warp whose wait gave up leaves the loop at the
       // same step as all the others
       if (PAIR && paired) ok = bar_and(1, 32 * C::kComputeWarps, ok);
     }
+    // the deferred additions still pending (those of the step before, for
+    // the pipelined d = 64 path, whose phase 2 then runs the last time)
+    if (kDefer && pend_dst != nullptr) red_groups<kDeferG>(pend_dst + (kG - kDeferG) * 128, pend);
+    pend_dst = nullptr;
+    if (kPipe && ok && n_steps > 0) ok = phase2(n_steps - 1);
     if (kDefer && pend_dst != nullptr) red_groups<kDeferG>(pend_dst + (kG - kDeferG) * 128, pend);
     // epilogue: dK (times scale) and dV of this quadrant's keys; 32 columns
     // each: d = 128, slice cs of both; d = 64, slices 0-1 take dK and 2-3 dV
