@@ -500,9 +500,9 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     // the second, so that the first half's dV and dK products overlap the
     // second half's softmax; then a quarter of dQ's columns for the
     // query rows of its quadrant (32 at d = 128, 16 at d = 64; the CTA pairs
-    // read 32 with warps cs < 2 at d = 64).  The two phases of a step never
-    // overlap (the next dP^T waits for dQ at d = 128), so one pool of warps
-    // runs both.
+    // read 32 with warps cs < 2 at d = 64).  One pool of warps runs both
+    // phases: at d = 128 the next dP^T waits for the dQ read-out, and at
+    // d = 64 (kPipe) a step's dQ is read out after the next step's softmax.
     const int w = warp - 4;
     const int qd = w & 3, cs = w >> 2;
     const int row = qd * 32 + static_cast<int>(lane);  // key (phase 1) / query (phase 2)
