@@ -88,23 +88,29 @@ struct BwdCfg {
   static_assert(D == 64 || D == 128, "head dim must be 64 or 128");
   static constexpr int kTile = 128 * D * 2;   // one 128-row tile of 16-bit elements
   static constexpr int kHalf = 128 * 64 * 2;  // 64 columns of 128 rows: one swizzle span
+  // depth of the Q/dO ring: at d = 64 the next step's first query half of
+  // S^T and dP^T is issued one query half into the step, so its Q and dO
+  // must be loaded a stage earlier; d = 128 has room for two
+  static constexpr int kStages = D == 64 ? 3 : 2;
   static constexpr int kK = 0, kV = kTile;
-  static constexpr int kQ = 2 * kTile;        // two stages
-  static constexpr int kDO = kQ + 2 * kTile;  // two stages
-  static constexpr int kDS = kDO + 2 * kTile; // dS^T, [query half][128 key rows][128 bytes]
-  static constexpr int kLse = kDS + 2 * kHalf;  // [stage][128] fp32
-  static constexpr int kDd = kLse + 2 * 512;    // [stage][128] fp32
-  static constexpr int kBar = kDd + 2 * 512;
-  // barriers: K/V loaded; Q/dO stage full (2) and empty (2); S^T and dP^T
+  static constexpr int kQ = 2 * kTile;
+  static constexpr int kDO = kQ + kStages * kTile;
+  static constexpr int kDS = kDO + kStages * kTile;  // dS^T, [query half][128 key rows][128 bytes]
+  static constexpr int kLse = kDS + 2 * kHalf;        // [stage][128] fp32
+  static constexpr int kDd = kLse + kStages * 512;    // [stage][128] fp32
+  static constexpr int kBar = kDd + kStages * 512;
+  // barriers: K/V loaded; Q/dO stage full and empty (one each per stage); S^T and dP^T
   // done; dS written and dQ read (one arrival per compute warp each); dQ
   // done; dK/dV done; drain; for CTA pairs: the peer may write into this
   // CTA's dS buffer (arrived by the peer), the peer's dQ columns have landed
   // there (one local arrival + the bytes); and the first half of the query
   // columns' P^T and dS^T written (one arrival per compute warp); and (d =
-  // 64) a step's second-half dV and dK done (an MMA commit)
-  static constexpr int bKV = 0, bFull = 1, bEmpty = 3, bSdp = 5, bDs = 6, bDqFull = 7,
-                       bDqFree = 8, bDkdv = 9, bDrain = 10, bSendOk = 11, bRecv = 12,
-                       bDsA = 13, bTail = 14, kNumBars = 15;
+  // 64) a step's second-half dV and dK done (an MMA commit), and S^T and
+  // dP^T of the first query half done (bSdp then covers the second half)
+  static constexpr int bKV = 0, bFull = 1, bEmpty = 1 + kStages, bSdp = 1 + 2 * kStages,
+                       bDs = bSdp + 1, bDqFull = bSdp + 2, bDqFree = bSdp + 3, bDkdv = bSdp + 4,
+                       bDrain = bSdp + 5, bSendOk = bSdp + 6, bRecv = bSdp + 7, bDsA = bSdp + 8,
+                       bTail = bSdp + 9, bSdpA = bSdp + 10, kNumBars = bSdp + 11;
   static constexpr uint32_t kRecvBytes = 128 * (D / 2) * 4;  // half of dQ's columns, fp32
   static constexpr int kMisc = kBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kUsed = kMisc + 16;
@@ -123,6 +129,7 @@ struct BwdCfg {
   static constexpr uint32_t cP2 = 256 + 3 * D;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kIdescS = idesc_f16(BF16, false, 128, 128);         // S^T, dP^T
+  static constexpr uint32_t kIdescSh = idesc_f16(BF16, false, 128, 64);          // one query half
   static constexpr uint32_t kIdescG = idesc_f16(BF16, true, 128, D);            // dV, dK
   static constexpr uint32_t kIdescQ = idesc_f16_ab(BF16, true, true, 128, D);   // dQ
   static constexpr int kThreads = 640;
@@ -298,11 +305,12 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::bKV), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar(C::bFull + s), 1);
       mbar_init(bar(C::bEmpty + s), 1);
     }
     mbar_init(bar(C::bSdp), 1);
+    mbar_init(bar(C::bSdpA), 1);
     mbar_init(bar(C::bDs), C::kComputeWarps);      // one arrival per compute warp
     mbar_init(bar(C::bDsA), C::kComputeWarps);     // the same, first query half
     mbar_init(bar(C::bTail), 1);
@@ -344,8 +352,10 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       }
       int issued = 0;
       for (int t = 0; t < n_steps; ++t) {
-        const int s = t & 1;
-        if (t >= 2 && !wait_bar(bar(C::bEmpty + s), ((t >> 1) + 1) & 1u, abort_flag, p.status)) break;
+        const int s = t % C::kStages;
+        if (t >= C::kStages &&
+            !wait_bar(bar(C::bEmpty + s), ((t / C::kStages) + 1) & 1u, abort_flag, p.status))
+          break;
         const int i = i0 + t;
         mbar_arrive_expect_tx(bar(C::bFull + s), 2 * C::kTile + 1024);
         for (int h = 0; h < D / 64; ++h) {
@@ -361,8 +371,8 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       }
       // drain: every issued copy lands before shared memory is released
       wait_drain(bar(C::bKV), 0, abort_flag, p.status);
-      for (int s = 0; s < 2; ++s) {
-        const int cnt = (issued - s + 1) / 2;  // loads into stage s
+      for (int s = 0; s < C::kStages; ++s) {
+        const int cnt = (issued - s + C::kStages - 1) / C::kStages;  // loads into stage s
         if (cnt > 0) wait_drain(bar(C::bFull + s), (cnt - 1) & 1u, abort_flag, p.status);
       }
     }
@@ -383,19 +393,28 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     };
     bool ok = wait_bar(bar(C::bKV), 0, abort_flag, p.status);
     if constexpr (kPipe) {
-      // S^T(t) and dP^T(t) of a step, once its Q and dO are loaded
-      auto issue_sdp = [&](int tt) -> bool {
-        const int st = tt & 1;
-        if (!wait_bar(bar(C::bFull + st), (tt >> 1) & 1u, abort_flag, p.status)) return false;
-        tc_fence_after();
-        ss_kk(C::cS, sbase + C::kK, sbase + C::kQ + st * C::kTile, C::kIdescS, D / 16, false);
-        ss_kk(C::cDP, sbase + C::kV, sbase + C::kDO + st * C::kTile, C::kIdescS, D / 16, false);
-        mma_commit_if(leader, bar(C::bSdp));
+      // S^T(t) and dP^T(t) of one query half h of a step (queries [64 h,
+      // 64 h + 64): N = 64, B = rows 64 h.. of the Q and dO tiles, one
+      // 128-byte row each at d = 64), once its Q and dO are loaded; the
+      // first half's completion is bSdpA, the second's bSdp
+      auto issue_sdp = [&](int tt, int h) -> bool {
+        const int st = tt % C::kStages;
+        if (h == 0) {
+          if (!wait_bar(bar(C::bFull + st), (tt / C::kStages) & 1u, abort_flag, p.status))
+            return false;
+          tc_fence_after();
+        }
+        const uint32_t rows = static_cast<uint32_t>(h) * 64u * 128u;
+        ss_kk(C::cS + 64 * h, sbase + C::kK, sbase + C::kQ + st * C::kTile + rows, C::kIdescSh,
+              D / 16, false);
+        ss_kk(C::cDP + 64 * h, sbase + C::kV, sbase + C::kDO + st * C::kTile + rows, C::kIdescSh,
+              D / 16, false);
+        mma_commit_if(leader, bar(h ? C::bSdp : C::bSdpA));
         return true;
       };
-      if (ok && n_steps > 0) ok = issue_sdp(0);
+      if (ok && n_steps > 0) ok = issue_sdp(0, 0) && issue_sdp(0, 1);
       for (int t = 0; ok && t < n_steps; ++t) {
-        const int s = t & 1;
+        const int s = t % C::kStages;
         const uint32_t q_s = sbase + C::kQ + s * C::kTile, do_s = sbase + C::kDO + s * C::kTile;
         const uint64_t bdo = mdesc0 + desc_addr(do_s), bq = mdesc0 + desc_addr(q_s);
         const uint64_t ads = kdesc0 + desc_addr(sbase + C::kDS);
@@ -408,11 +427,14 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
         for (int kk = 0; kk < 4; ++kk)
           mma_ss_if(leader, tmem + C::cDK, ads + ((kk * 32) >> 4), bq + kk * (2048 >> 4),
                     C::kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
+        // the next step's first query half of S^T (its columns are free:
+        // the first half's dV above read the P^T packed there) and dP^T
+        // (read by this step's first half of the softmax)
+        if (t + 1 < n_steps && !(ok = issue_sdp(t + 1, 0))) break;
         if (!(ok = wait_bar(bar(C::bDs), t & 1u, abort_flag, p.status))) break;
         tc_fence_after();
-        // the next step's S^T (S is free: the first half's dV above read
-        // its P^T) and dP^T (read by this step's softmax)
-        if (t + 1 < n_steps && !(ok = issue_sdp(t + 1))) break;
+        // and its second half, read by this step's second half of the softmax
+        if (t + 1 < n_steps && !(ok = issue_sdp(t + 1, 1))) break;
         if (t > 0) {  // dQ(t-1) read out of its columns
           if (!(ok = wait_bar(bar(C::bDqFree), (t - 1) & 1u, abort_flag, p.status))) break;
           tc_fence_after();
@@ -435,9 +457,9 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
       }
     } else {
     for (int t = 0; ok && t < n_steps; ++t) {
-      const int s = t & 1;
+      const int s = t % C::kStages;
       const uint32_t q_s = sbase + C::kQ + s * C::kTile, do_s = sbase + C::kDO + s * C::kTile;
-      if (!(ok = wait_bar(bar(C::bFull + s), (t >> 1) & 1u, abort_flag, p.status))) break;
+      if (!(ok = wait_bar(bar(C::bFull + s), (t / C::kStages) & 1u, abort_flag, p.status))) break;
       tc_fence_after();
       ss_kk(C::cS, sbase + C::kK, q_s, C::kIdescS, D / 16, false);     // S^T = K Q^T
       if (C::kDqAliasDp && t > 0) {  // dQ(t-1) read out of the dP columns
@@ -607,10 +629,11 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
     };
     bool ok = true;
     for (int t = 0; ok && t < n_steps; ++t) {
-      ok = wait_bar(bar(C::bSdp), t & 1u, abort_flag, p.status);
+      // kPipe: each query half's S^T and dP^T has a barrier of its own
+      ok = wait_bar(bar(kPipe ? C::bSdpA : C::bSdp), t & 1u, abort_flag, p.status);
       if (ok) {
       tc_fence_after();
-      const int s = t & 1, i = i0 + t;
+      const int s = t % C::kStages, i = i0 + t;
       const float *lse2s = reinterpret_cast<const float *>(smem + C::kLse + s * 512);
       const float *dds = reinterpret_cast<const float *>(smem + C::kDd + s * 512);
       const bool diag = p.causal && i == jb;
@@ -618,6 +641,10 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
 #pragma unroll
       for (int sc = 0; sc < 2; ++sc) {
         const int q0 = 16 * cs + 64 * sc;  // first query column of this sub-chunk
+        if (kPipe && sc == 1) {
+          if (!wait_bar(bar(C::bSdp), t & 1u, abort_flag, p.status)) ok = false;
+          tc_fence_after();
+        }
         uint32_t sr[16], dr[16];
         tmem_ld16(t_lane + C::cS + q0, sr);
         tmem_ld16(t_lane + C::cDP + q0, dr);
