@@ -72,6 +72,10 @@ SMALL = [
     (2, 1, 1000, 128, torch.float16),
     (1, 2, 2048 + 77, 128, torch.bfloat16),
     (2, 2, 1024, 64, torch.bfloat16),
+    # d = 64 walks its three-stage Q/dO ring: two steps (fewer than the
+    # stages), and six with a ragged tail (the ring wraps twice)
+    (1, 1, 200, 64, torch.bfloat16),
+    (1, 2, 5 * 128 + 19, 64, torch.float16),
 ]
 
 
