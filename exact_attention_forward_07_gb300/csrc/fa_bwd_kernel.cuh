@@ -266,10 +266,12 @@ __global__ void __launch_bounds__(BwdCfg<D, BF16>::kThreads, 1)
   using C = BwdCfg<D, BF16>;
   // d = 64 (one CTA per key block): steps overlap.  With the second query
   // half's P^T in its own tensor-memory columns, the next step's S^T and
-  // dP^T go to the tensor core as soon as this step's dS is complete, ahead
-  // of this step's dQ and second-half dV and dK, and the compute warps form
-  // the next step's P^T and dS^T while those run; they read out this
-  // step's dQ after that.
+  // dP^T go to the tensor core one query half at a time: the first half
+  // once this step's first half of P^T and dS^T is formed (after this
+  // step's first-half dV and dK), the second once dS is complete (ahead of
+  // this step's dQ and second-half dV and dK).  The compute warps form the
+  // next step's P^T and dS^T while those run, and read out this step's dQ
+  // after that.
   constexpr bool kPipe = (D == 64) && !PAIR;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
