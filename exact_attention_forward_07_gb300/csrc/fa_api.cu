@@ -437,8 +437,22 @@ int launch(DeviceState &ds, int slot, const void *q, const void *k, const void *
   }
 
   const int grid = p.n_units < ds.sm_count ? p.n_units : ds.sm_count;
-  kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
-  cudaError_t e = cudaGetLastError();
+  // Programmatic dependent launch: the CTAs may be scheduled, and run
+  // their prologue (barriers, tensor memory), while the previous kernel in
+  // the stream drains; the kernel waits for that kernel's completion before
+  // its first global memory access, so stream order holds for the data.
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>(grid));
+  lc.blockDim = dim3(C::kThreads);
+  lc.dynamicSmemBytes = C::kSmemBytes;
+  lc.stream = stream;
+  cudaLaunchAttribute la[1];
+  la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  la[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = la;
+  lc.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&lc, kernel, tq, tk, tv, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (scratch != nullptr) cudaFreeAsync(scratch, stream);
   if (e != cudaSuccess) {
     if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)

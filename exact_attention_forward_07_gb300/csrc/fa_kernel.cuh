@@ -403,6 +403,12 @@ __global__ void __launch_bounds__(Cfg<D, BF16, STAGES, EXPSPLIT, STATS>::kThread
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_base_slot;
+  // launched as a programmatic dependent: nothing above touches global
+  // memory; wait here for the previous kernel in the stream to complete
+  // (and its writes to be visible), then let the next one be scheduled (its
+  // CTAs take SMs only as this grid's CTAs leave them, and wait likewise)
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp >= C::kSoftmaxWarps) {
     // Each role's code sits under its own setmaxnreg, so the compiler sizes

@@ -291,6 +291,15 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Programmatic dependent launch (a kernel launched with the programmatic
+// stream serialization attribute): wait until the grids it depends on have
+// completed and their memory is visible; allow the dependent grids to be
+// scheduled.  Both are no-ops in a kernel launched without the attribute.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Per-warpgroup register budget changes (all four warps of the warpgroup
 // execute them).  The sum over warpgroups must not exceed the launch's.
 template <uint32_t N>

@@ -102,7 +102,11 @@ typedef void *fa_stream_t;
  *   causal  : nonzero => query i sees keys 0..i only (top-left aligned)
  *   scale   : multiplies Q K^T before the mask and softmax; finite, > 0
  *             (usually 1/sqrt(d))
- *   stream  : cudaStream_t to launch on
+ *   stream  : cudaStream_t to launch on.  The kernel is launched as a
+ *             programmatic dependent of the previous kernel in the stream:
+ *             its CTAs may start while that kernel drains, but each waits
+ *             for its completion before touching memory, so the call is
+ *             ordered in the stream like any other launch.
  */
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
            int64_t H, int64_t N, int64_t d, int causal, float scale, fa_stream_t stream);
